@@ -1,0 +1,436 @@
+"""Benchmark of the streaming-attention hot path on one GB300 (or N replicas).
+
+One step = one pass of the whole path:
+  1. kv_stream_insert     on the scale-up workload (36 layer caches,
+                          prefix 512 + 6 views x 8 frames x 256 tokens),
+  2. stream_attn_prefill  of its 1536 new-frame queries x 32 heads per layer,
+  3. stream_attn_verify   of a 9-token block on the Alpamayo-shaped cache
+                          (prefix 256 + 4 x 4 x 180, 16 tail tokens), batch 64,
+                          with the greedy accept-length reduction.
+
+The reported value is the prefill attention's algorithmic TFLOP/s over the
+whole step (unmasked query-key pairs only, 4*d FLOP each); the verify
+kernel's HBM GB/s and the insert's GB/s are reported beside it.  Inputs stay
+resident in HBM; the caches (about 2.8 GB) are far larger than L2, so
+consecutive steps cannot hit in L2.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from streaming_kv_cache_gb300 import synth  # noqa: E402
+
+METRIC = "stream-prefill attn TFLOP/s (% bf16 peak); verify-step HBM GB/s (% peak)"
+PREFILL_W = synth.WORKLOADS["scaleup_36L"]
+VERIFY_W = synth.WORKLOADS["alpamayo_verify"]          # batch 64
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ---------------------------------------------------------------------------
+# algorithmic work
+
+def prefill_pairs(w) -> int:
+    """Visible (query, key) pairs per query head and cache: new-frame token
+    (v, t) sees every key with logical index <= P + v*F*T + (F-1)*T + t."""
+    tot = 0
+    for v in range(w.V):
+        base = w.P + v * w.F * w.T + (w.F - 1) * w.T + 1
+        tot += w.T * base + w.T * (w.T - 1) // 2
+    return tot
+
+
+def prefill_flop(w) -> float:
+    return 4.0 * w.d * w.Hq * w.C * prefill_pairs(w)
+
+
+def verify_bytes(w) -> float:
+    """Per launch: K and V of every visible key once per (cache, kv head),
+    the block's Q in and O out, the block K/V read and written to the tail."""
+    keys = w.P + w.V * w.F * w.T + w.tail_len + w.blk
+    kv = 2.0 * keys * w.d * 2 * w.Hkv
+    q_o = 2.0 * w.blk * w.Hq * w.d * 2
+    blk_kv = 2.0 * 2 * w.blk * w.Hkv * w.d * 2
+    return w.C * (kv + q_o + blk_kv)
+
+
+def insert_bytes(w) -> float:
+    return 2.0 * 2 * w.C * w.V * w.T * w.Hkv * w.d * 2   # K and V, read + write
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(PEAKS_FALLBACK), "fallback"
+
+
+def traffic_for(kernel_file: str):
+    """Per-launch DRAM bytes from the committed ncu summary, or None when the
+    kernel source changed since the counters were taken."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    ent = d.get(kernel_file)
+    if not ent:
+        return None
+    src = os.path.join(ROOT, "streaming_kv_cache_gb300", "csrc", kernel_file)
+    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    return ent["bytes_per_launch"] if ent.get("source_sha") == h else None
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index, self.proc, self.lines = index, None, []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = max(mx, float(f[2]))
+            except ValueError:
+                continue
+            for n, val in zip(names, f[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx or None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# the CPU oracle as a bounded-sample baseline
+
+def oracle_sample(seconds: float = 12.0):
+    """Time the fp64 oracle on a bounded sample of the prefill workload: one
+    layer cache, a spread of new-frame query rows (all 32 heads, full
+    recompute over the 12,800-key window).  Returns (TFLOP/s, cores, text)."""
+    from oracle import skv_oracle as O
+    w = PREFILL_W.with_(C=1)
+    pk, pv = synth.prefix_kv(w, "cpu")
+    win = O.StreamWindow(w.P, w.V, w.F, w.T, w.Hkv, w.d, pk[0], pv[0])
+    for i in range(w.F + 1):
+        k, v = synth.frame_kv(w, i, "cpu")
+        win.insert(k[0], v[0])
+    q = synth.frame_q(w, w.F, "cpu")[0]
+
+    def flop(rows):
+        return sum(4.0 * w.d * w.Hq * (win.new_frame_index(int(j) // w.T, int(j) % w.T) + 1)
+                   for j in rows)
+
+    n, spent, done_flop, calls = 8, 0.0, 0.0, 0
+    rng = np.random.default_rng(0)
+    while spent < seconds and calls < 64:
+        rows = np.sort(rng.choice(w.n_new, size=min(n, w.n_new), replace=False))
+        t0 = time.perf_counter()
+        O.stream_prefill(win, q, w.theta, w.sm_scale, rows=rows)
+        dt = time.perf_counter() - t0
+        spent += dt
+        done_flop += flop(rows)
+        calls += 1
+        n = min(w.n_new, n * 2) if dt < seconds / 8 else n
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    text = ("fp64 NumPy oracle, %d prefill calls on one layer cache of the scale-up workload "
+            "(%.0f query rows x 32 heads in total, full recompute over the 12,800-key window), "
+            "%.1f s" % (calls, done_flop / (4.0 * w.d * w.Hq * 7000), spent))
+    return done_flop / spent / 1e12, cores, text, spent
+
+
+# ---------------------------------------------------------------------------
+
+def emit(obj):
+    print(json.dumps(obj), flush=True)
+
+
+def run_reference(args, rank, world):
+    """The reference arm: the oracle, as it stands, on the host cores."""
+    if rank != 0:
+        return
+    per_step = max(2.0, 60.0 / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        oracle_sample(seconds=min(per_step, 3.0))
+    vals, secs, cores, text = [], 0.0, 1, ""
+    for _ in range(args.steps):
+        v, cores, text, sp = oracle_sample(seconds=per_step)
+        vals.append(v)
+        secs += sp
+    value = statistics.median(vals)
+    emit({"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+          "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+          "ms_per_step": 1e3 * secs / max(1, args.steps), "higher_is_better": True,
+          "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+          "config": {"workload": "scaleup_36L prefill sample on the host (oracle)"},
+          "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                           "sample": text},
+          "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                  "d2h_bytes_per_step": 0}})
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+
+    import torch
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+
+    from streaming_kv_cache_gb300 import build as B
+    if rank == 0:
+        B.build()
+    if dist:
+        dist.barrier()
+    from streaming_kv_cache_gb300 import skv
+
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(1234 + rank)
+
+    def randn(shape, scale=1.0):
+        return (torch.randn(shape, generator=gen, device=dev, dtype=torch.float32) * scale).to(torch.bfloat16)
+
+    # scale-up streaming workload: prefix + full window, then one step per iteration
+    pw = PREFILL_W
+    pc = skv.StreamCache(pw.C, pw.P, pw.V, pw.F, pw.T, pw.Hkv, pw.d, pw.theta, tail_cap=pw.tail_cap)
+    skv.kv_write_rows(pc, 0, randn((pw.C, pw.P, pw.Hkv, pw.d)), randn((pw.C, pw.P, pw.Hkv, pw.d)))
+    k_new = randn((pw.C, pw.V, pw.T, pw.Hkv, pw.d))
+    v_new = randn((pw.C, pw.V, pw.T, pw.Hkv, pw.d))
+    for _ in range(pw.F):
+        skv.kv_stream_insert(pc, k_new, v_new)
+    q_new = randn((pw.C, pw.n_new, pw.Hq, pw.d), pw.q_scale)
+    p_out = torch.empty_like(q_new)
+
+    # verify workload: Alpamayo-shaped cache x 64, 16 tail tokens, 9-token block
+    vw = VERIFY_W
+    vc = skv.StreamCache(vw.C, vw.P, vw.V, vw.F, vw.T, vw.Hkv, vw.d, vw.theta, tail_cap=vw.tail_cap)
+    skv.kv_write_rows(vc, 0, randn((vw.C, vw.P, vw.Hkv, vw.d)), randn((vw.C, vw.P, vw.Hkv, vw.d)))
+    vk = randn((vw.C, vw.V, vw.T, vw.Hkv, vw.d))
+    for _ in range(vw.F):
+        skv.kv_stream_insert(vc, vk, vk)
+    skv.kv_write_rows(vc, vc.n_visual, randn((vw.C, vw.tail_len, vw.Hkv, vw.d)),
+                      randn((vw.C, vw.tail_len, vw.Hkv, vw.d)))
+    q_blk = randn((vw.C, vw.blk, vw.Hq, vw.d), vw.q_scale)
+    k_blk = randn((vw.C, vw.blk, vw.Hkv, vw.d))
+    v_blk = randn((vw.C, vw.blk, vw.Hkv, vw.d))
+    tgt, drf, _ = synth.planted_ids(vw.C, vw.blk, "bench")
+    tgt_d, drf_d = torch.from_numpy(tgt).to(dev), torch.from_numpy(drf).to(dev)
+    tail0 = torch.full((vw.C,), vw.tail_len, dtype=torch.int32, device=dev)
+    ws = skv.verify_workspace(vc, vw.Hq, vw.blk)
+    v_out = torch.empty_like(q_blk)
+    acc = torch.empty((vw.C,), dtype=torch.int32, device=dev)
+    nxt = torch.empty((vw.C,), dtype=torch.int32, device=dev)
+    torch.cuda.synchronize()
+
+    launches_per_step = 1 + 1 + 3      # insert; prefill; verify tail write + attention + accept
+    ev = {n: [] for n in ("insert", "prefill", "verify")}
+
+    def step(record):
+        if record:
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+            e[0].record()
+        skv.kv_stream_insert(pc, k_new, v_new)
+        if record:
+            e[1].record()
+        skv.stream_attn_prefill(pc, q_new, pw.sm_scale, out=p_out)
+        if record:
+            e[2].record()
+        skv.stream_attn_verify(vc, tail0, q_blk, k_blk, v_blk, vw.sm_scale, target_ids=tgt_d,
+                               draft_ids=drf_d, ws=ws, out=v_out, accept_len=acc, next_token=nxt)
+        if record:
+            e[3].record()
+            ev["insert"].append((e[0], e[1]))
+            ev["prefill"].append((e[1], e[2]))
+            ev["verify"].append((e[2], e[3]))
+
+    for _ in range(args.warmup):
+        step(False)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        start.record()
+        for _ in range(args.steps):
+            step(True)
+        stop.record()
+        torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    t_ms = start.elapsed_time(stop)
+    status = pc.device_status() | vc.device_status()
+    if status:
+        raise RuntimeError("device status %d during the bench: %s" % (status, skv.status_string(status)))
+
+    def avg(name):
+        return statistics.mean(a.elapsed_time(b) for a, b in ev[name])
+
+    k_ms = {n: avg(n) for n in ev}
+
+    # --- end to end through host buffers (pinned), same step, same metric
+    h_k = k_new.cpu().pin_memory(); h_v = v_new.cpu().pin_memory(); h_q = q_new.cpu().pin_memory()
+    h_qb = q_blk.cpu().pin_memory(); h_kb = k_blk.cpu().pin_memory(); h_vb = v_blk.cpu().pin_memory()
+    h_t = torch.from_numpy(tgt).pin_memory(); h_d = torch.from_numpy(drf).pin_memory()
+    h_out = torch.empty(p_out.shape, dtype=p_out.dtype).pin_memory()
+    h_vout = torch.empty(v_out.shape, dtype=v_out.dtype).pin_memory()
+    h_acc = torch.empty(acc.shape, dtype=acc.dtype).pin_memory()
+    h_nxt = torch.empty(nxt.shape, dtype=nxt.dtype).pin_memory()
+    ins = [h_k, h_v, h_q, h_qb, h_kb, h_vb, h_t, h_d]
+    outs = [h_out, h_vout, h_acc, h_nxt]
+    h2d = sum(t.numel() * t.element_size() for t in ins)
+    d2h = sum(t.numel() * t.element_size() for t in outs)
+
+    def e2e_step():
+        k_new.copy_(h_k, non_blocking=True); v_new.copy_(h_v, non_blocking=True)
+        q_new.copy_(h_q, non_blocking=True); q_blk.copy_(h_qb, non_blocking=True)
+        k_blk.copy_(h_kb, non_blocking=True); v_blk.copy_(h_vb, non_blocking=True)
+        tgt_d.copy_(h_t, non_blocking=True); drf_d.copy_(h_d, non_blocking=True)
+        step(False)
+        h_out.copy_(p_out, non_blocking=True); h_vout.copy_(v_out, non_blocking=True)
+        h_acc.copy_(acc, non_blocking=True); h_nxt.copy_(nxt, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    s2, t2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s2.record()
+    for _ in range(args.steps):
+        e2e_step()
+    t2.record()
+    torch.cuda.synchronize()
+    e2e_ms = s2.elapsed_time(t2)
+
+    # max over ranks
+    if dist:
+        tt = torch.tensor([t_ms, e2e_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_ms, e2e_ms = float(tt[0]), float(tt[1])
+
+    flop = prefill_flop(pw)
+    ms_per_step = t_ms / args.steps
+    value = world * flop * args.steps / (t_ms * 1e-3) / 1e12
+    e2e_value = world * flop * args.steps / (e2e_ms * 1e-3) / 1e12
+    pk, src = peaks()
+    pre_tf = flop / (k_ms["prefill"] * 1e-3) / 1e12
+    ver_gbs = verify_bytes(vw) / (k_ms["verify"] * 1e-3) / 1e9
+    ins_gbs = insert_bytes(pw) / (k_ms["insert"] * 1e-3) / 1e9
+    tag = "of measured" if src == "measured" else "of fallback"
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        v, cores, text, _ = oracle_sample()
+        cpu = {"value": v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": text}
+
+    if rank == 0:
+        emit({
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": "scaleup_36L step (insert + prefill, 36 layer caches, P=512, "
+                                   "6 views x 8 frames x 256 tokens, 1536 queries, Hq=32/Hkv=8/d=128) "
+                                   "+ alpamayo_verify (B=64, 9-token block, 16 tail tokens)",
+                       "l2": "inputs larger than L2 (caches 2.8 GB), no flush",
+                       "prefill_gflop_per_step": flop / 1e9,
+                       "verify_mb_per_step": verify_bytes(vw) / 1e6,
+                       "insert_mb_per_step": insert_bytes(pw) / 1e6},
+            "kernels_ms": k_ms,
+            "roofline": {"bound": "tensor", "kernel": "stream_attn_prefill", "achieved": pre_tf,
+                         "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                         "frac": pre_tf / pk["bf16_tflops"], "peak_source": tag + " (burst)",
+                         "frac_of_sustained": pre_tf / pk["bf16_tflops_sustained"],
+                         "traffic": traffic_for("attn_simple.cu")},
+            "verify_roofline": {"bound": "hbm", "kernel": "stream_attn_verify", "achieved": ver_gbs,
+                                "peak": pk["hbm_gbs"], "unit": "GB/s",
+                                "frac": ver_gbs / pk["hbm_gbs"], "peak_source": tag},
+            "insert_roofline": {"bound": "hbm", "kernel": "kv_stream_insert", "achieved": ins_gbs,
+                                "peak": pk["hbm_gbs"], "unit": "GB/s",
+                                "frac": ins_gbs / pk["hbm_gbs"], "peak_source": tag},
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / args.steps},
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clk.summary(),
+        })
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,215 @@
+/*
+ * skv.h -- C ABI of libskv: streaming view-major KV-cache attention on GB300
+ * (sm_103a).
+ *
+ * The operation (FlashDrive, Flash Vision-Language-Action Inference for
+ * Autonomous Driving; blog walkthrough section 3 "Encode & Prefill: Streaming
+ * Inference" and paper summary "Streaming Inference"): a VLA model looks at a
+ * sliding window of F frames from each of V camera views.  Every step the
+ * window advances by one frame per view, so only the newest frame is new.
+ * The cache keeps the keys WITHOUT rotary embedding (pre-RoPE) and rotates
+ * each key at its current logical position inside the attention kernel,
+ * because that position moves as older frames are evicted (blog section 3.3
+ * "RoPE Position Shift").  Tokens are ordered view-major -- the system prefix,
+ * then view 0's frames oldest to newest, view 1's, ..., then the reasoning
+ * tail (blog section 3.2 "View-Major Ordering") -- and a query sees a key iff
+ * the key's logical index is at most its own.
+ *
+ * Conventions shared by every call:
+ *  - All pointers named "device" are CUDA device pointers owned by the
+ *    caller.  The library never allocates, never frees and never keeps a
+ *    pointer after a call returns.
+ *  - bf16 tensors are raw 16-bit brain-float arrays, C-contiguous, in the
+ *    layout stated beside them; every device pointer must be 16-byte
+ *    aligned.
+ *  - `stream` is a cudaStream_t passed as void*.  Calls only enqueue work on
+ *    it, never synchronise and never copy to or from the host, so they may
+ *    be captured into a CUDA graph.
+ *  - A call returns SKV_OK after enqueueing, or a negative SKV_ERR_* code
+ *    and enqueues nothing.  Errors found on the device while the kernels run
+ *    (a bounded wait that gave up, a ring head out of range, a tail that
+ *    would overflow) are OR-ed into the int32 device word cache->status as
+ *    SKV_DEV_* bits; the caller reads it when it wants to.
+ */
+#ifndef SKV_H_
+#define SKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SKV_VERSION 1
+
+/* host-side return codes */
+#define SKV_OK 0
+#define SKV_ERR_INVALID (-1)     /* null/misaligned pointer, bad shape or argument */
+#define SKV_ERR_UNSUPPORTED (-2) /* no sm_103 device current, or shape outside what the kernels cover */
+#define SKV_ERR_CUDA (-3)        /* a CUDA runtime/driver call failed; see skv_last_cuda_error() */
+
+/* device status bits (OR-ed into *cache->status) */
+#define SKV_DEV_TIMEOUT 1        /* a bounded wait inside a kernel gave up; outputs are undefined */
+#define SKV_DEV_BAD_HEAD 2       /* a ring head was outside [0, F); that cache was skipped */
+#define SKV_DEV_TAIL_OVERFLOW 4  /* tail_len + blk > tail_cap in verify; that cache was skipped */
+#define SKV_DEV_BAD_TAIL 8       /* tail_len < 0 in verify; that cache was skipped */
+
+/*
+ * One set of C independent caches (model layers x batch) of identical
+ * geometry.  Per cache c and kv head h there are row_cap key rows:
+ *
+ *   rows [0, P)                      system prefix, logical index = row
+ *   rows [P, P + V*F*T)              the ring: view v, slot s, token t at
+ *                                    row P + (v*F + s)*T + t
+ *   rows [P + V*F*T, ... + tail_cap) reasoning-token tail, index = row
+ *
+ * The ring of view v holds its F frames in F slots; head[c][v] is the slot
+ * of the oldest frame, so logical frame f (0 = oldest) sits in slot
+ * (head + f) mod F and a ring key's logical index is P + v*F*T + f*T + t.
+ * Inserting a frame overwrites the oldest slot and advances the head; no
+ * data moves.
+ *
+ * k   device bf16 [C][Hkv][row_cap][d]  pre-RoPE keys, one row per token
+ * vt  device bf16 [C][Hkv][d][row_cap]  values, stored transposed (dimension-
+ *                                       major) so that both tensor-core
+ *                                       products read K-major operands
+ * head    device int32 [C][V]   ring heads (0 for an empty cache)
+ * sync    device int32 [C][V]   zero-initialised counters used by
+ *                               kv_stream_insert; the call leaves them at 0
+ * rope    device fp32 [rope_len][d/2][2]  (cos, sin) of position*theta^(-2i/d),
+ *                               filled by skv_build_rope_table; rope_len must
+ *                               cover every logical index (P + V*F*T + tail_cap)
+ * status  device int32 [1]      SKV_DEV_* bits, OR-ed in by the kernels
+ *
+ * Every row of k and vt must hold finite values (allocate them zeroed):
+ * masked keys still pass through the tensor cores with weight 0.
+ */
+typedef struct skv_cache {
+  int32_t n_cache;    /* C */
+  int32_t n_view;     /* V >= 1 */
+  int32_t n_frame;    /* F >= 1 */
+  int32_t frame_len;  /* T >= 1 */
+  int32_t prefix_len; /* P >= 0 */
+  int32_t tail_cap;   /* rows reserved for reasoning tokens, >= 0 */
+  int32_t n_kv_head;  /* Hkv >= 1 */
+  int32_t head_dim;   /* d: 64 or 128 */
+  int32_t row_cap;    /* >= P + V*F*T + tail_cap, multiple of 8 */
+  int32_t rope_len;   /* rows of the rope table */
+  void* k;
+  void* vt;
+  int32_t* head;
+  int32_t* sync;
+  const float* rope;
+  int32_t* status;
+  uint64_t wait_ns;   /* limit of every bounded wait in a kernel; 0 = 2 s */
+} skv_cache;
+
+/* Library version (SKV_VERSION). */
+int skv_version(void);
+
+/* Human-readable text for an SKV_* return code or SKV_DEV_* bit set. */
+const char* skv_status_string(int code);
+
+/* The cudaError_t of the last call that returned SKV_ERR_CUDA on this host
+ * thread (0 if none). */
+int skv_last_cuda_error(void);
+
+/* Smallest valid row_cap for a geometry (rounded up to a multiple of 128). */
+int32_t skv_row_cap(int32_t P, int32_t V, int32_t F, int32_t T, int32_t tail_cap);
+
+/*
+ * Fill the rotary table used by every attention call:
+ * tab[p][i] = (cos(p * theta^(-2i/d)), sin(...)) for p < n_pos, i < d/2,
+ * angles formed and reduced in fp64 on the device, rounded once to fp32.
+ * tab: device fp32 [n_pos][d/2][2].  Pairs (i, i + d/2) of a head vector
+ * rotate together (rotate-half form).
+ */
+int skv_build_rope_table(float* tab, int32_t n_pos, int32_t head_dim, double theta,
+                         void* stream);
+
+/*
+ * Write n_rows token-major K/V rows into rows [row0, row0 + n_rows) of every
+ * cache and kv head, as they are (pre-RoPE).  Used to place the system
+ * prefix and reasoning-tail tokens; the ring is written by kv_stream_insert.
+ * k_src, v_src: device bf16 [C][n_rows][Hkv][d].  Bit-exact copy.
+ */
+int kv_write_rows(const skv_cache* cache, int32_t row0, int32_t n_rows, const void* k_src,
+                  const void* v_src, void* stream);
+
+/*
+ * kv_stream_insert -- one streaming step of the window (blog section 3.1:
+ * evict each view's oldest frame, keep the rest, add only the newest).
+ * For every cache c and view v: s = head[c][v]; the new frame's K/V are
+ * written into slot s (evicting the oldest frame); then head[c][v] =
+ * (s + 1) mod F.  Prefix, tail and every other slot are untouched.
+ * k_new, v_new: device bf16 [C][V][T][Hkv][d], token-major, pre-RoPE.
+ * Bit-exact.  The initial fill of an empty cache is F calls; attention is
+ * defined once the window is full (the first window only fills the cache).
+ * A head outside [0, F) sets SKV_DEV_BAD_HEAD and that (c, v) is skipped.
+ */
+int kv_stream_insert(const skv_cache* cache, const void* k_new, const void* v_new,
+                     void* stream);
+
+/*
+ * stream_attn_prefill -- attention of the newest frame's tokens over the
+ * window (blog sections 3.2-3.3).  Call it after kv_stream_insert, so the
+ * newest frame is in the cache.  Query token j = (view j / T, token j mod T
+ * of that view's newest frame) sits at logical index
+ * P + v*F*T + (F-1)*T + t and sees every key whose logical index is at most
+ * its own: the prefix, all earlier views, its own view's older frames and
+ * its own frame causally; never later views nor the tail.  Queries and keys
+ * are rotated (rotate-half RoPE from cache->rope) at their logical
+ * positions inside the kernel; query head h reads kv head h / (Hq/Hkv).
+ *
+ * q_new: device bf16 [C][V*T][Hq][d], pre-RoPE.
+ * out:   device bf16 [C][V*T][Hq][d]: softmax(sm_scale * q.k) v, fp32
+ *        accumulation, rounded to nearest even once.
+ * lse:   device fp32 [C][Hq][V*T] natural-log sum of exp of the scaled
+ *        scores, or NULL.
+ * Needs Hq % Hkv == 0 and 128 % (Hq/Hkv) == 0.
+ */
+int stream_attn_prefill(const skv_cache* cache, int32_t n_q_head, const void* q_new, void* out,
+                        float* lse, float sm_scale, void* stream);
+
+/* Bytes of device workspace stream_attn_verify needs for this geometry. */
+size_t skv_verify_workspace_bytes(const skv_cache* cache, int32_t n_q_head, int32_t blk);
+
+/*
+ * stream_attn_verify -- one speculative-verify pass (blog section 4.2,
+ * steps 1-4; VFlash "03 · Generalist decoding": the target checks a drafted
+ * block in one pass and keeps the longest matching prefix plus its own next
+ * token).
+ *
+ * Block token j (j < blk; token 0 = the last accepted token, 1.. = drafts)
+ * of cache c sits at logical index P + V*F*T + tail_len[c] + j.  The call
+ *  1. writes the block's pre-RoPE K/V into tail rows tail_len[c] + j;
+ *  2. attends each block query over the prefix, all frames, the tail
+ *     [0, tail_len[c]) and block tokens 0..j (causal within the block);
+ *  3. if target_ids and draft_ids are both non-NULL, sets accept_len[c] =
+ *     the largest k <= blk-1 with draft[c][i] == target[c][i-1] for all
+ *     1 <= i <= k, and next_token[c] = target[c][accept_len[c]].
+ * The caller then advances tail_len[c] by accept_len[c] + 1.
+ *
+ * tail_len: device int32 [C], tokens already in the tail.
+ * q_blk:    device bf16 [C][blk][Hq][d]; k_blk, v_blk: [C][blk][Hkv][d].
+ * out:      device bf16 [C][blk][Hq][d].
+ * target_ids, draft_ids: device int32 [C][blk] or NULL.
+ * accept_len, next_token: device int32 [C] (unused when ids are NULL).
+ * ws: device workspace of ws_bytes >= skv_verify_workspace_bytes(); it must
+ *     be zero-filled before its first use, the call leaves it ready for the
+ *     next one (re-zero it after a call that set a device status bit).
+ * Needs 1 <= blk, blk * (Hq/Hkv) <= 128.  tail_len + blk > tail_cap sets
+ * SKV_DEV_TAIL_OVERFLOW and skips that cache.
+ */
+int stream_attn_verify(const skv_cache* cache, int32_t n_q_head, int32_t blk,
+                       const int32_t* tail_len, const void* q_blk, const void* k_blk,
+                       const void* v_blk, void* out, const int32_t* target_ids,
+                       const int32_t* draft_ids, int32_t* accept_len, int32_t* next_token,
+                       void* ws, size_t ws_bytes, float sm_scale, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SKV_H_ */

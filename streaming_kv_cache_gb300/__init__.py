@@ -1,0 +1,10 @@
+"""streaming_kv_cache_gb300 -- streaming view-major KV-cache attention on GB300.
+
+A C-ABI library (libskv.so, hand-written CUDA for sm_103a) with three calls:
+kv_stream_insert, stream_attn_prefill and stream_attn_verify, plus a thin
+ctypes binding.  Build it with streaming_kv_cache_gb300.build.build().
+"""
+from . import synth  # noqa: F401
+from .skv import (EXPORTS, SkvError, StreamCache, kv_stream_insert, kv_write_rows,  # noqa: F401
+                  lib, skv_build_rope_table, skv_row_cap, skv_verify_workspace_bytes,
+                  status_string, stream_attn_prefill, stream_attn_verify, verify_workspace)

@@ -1,0 +1,63 @@
+// Shared device-side helpers of libskv: cache geometry, logical-index
+// arithmetic and bf16 conversions.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "skv.h"
+
+namespace skv {
+
+// Plain-value copy of the cache geometry that kernels receive by value.
+struct Geom {
+  int C, V, F, T, P, tail_cap, Hkv, d, row_cap, rope_len;
+  __host__ __device__ int ring_rows() const { return V * F * T; }
+  __host__ __device__ int n_visual() const { return P + V * F * T; }
+};
+
+inline Geom geom_of(const skv_cache& c) {
+  Geom g;
+  g.C = c.n_cache; g.V = c.n_view; g.F = c.n_frame; g.T = c.frame_len; g.P = c.prefix_len;
+  g.tail_cap = c.tail_cap; g.Hkv = c.n_kv_head; g.d = c.head_dim; g.row_cap = c.row_cap;
+  g.rope_len = c.rope_len;
+  return g;
+}
+
+// Logical index (= rotary position) of physical key row r of cache c, given
+// that cache's ring heads.  The prefix and the tail sit at their own row;
+// ring row P + (v*F + s)*T + t holds logical frame f = (s - head[v]) mod F
+// of view v, at index P + v*F*T + f*T + t.
+__device__ __forceinline__ int key_index(const Geom& g, const int* __restrict__ head_c, int r) {
+  const int u = r - g.P;
+  if (u < 0 || u >= g.ring_rows()) return r;
+  const int FT = g.F * g.T;
+  const int v = u / FT;
+  const int rem = u - v * FT;
+  const int s = rem / g.T;
+  const int t = rem - s * g.T;
+  int f = s - head_c[v];
+  if (f < 0) f += g.F;
+  return g.P + v * FT + f * g.T + t;
+}
+
+// Logical index of token t of view v's newest frame (the new-frame queries).
+__host__ __device__ __forceinline__ int new_frame_index(const Geom& g, int v, int t) {
+  return g.P + v * g.F * g.T + (g.F - 1) * g.T + t;
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Round two floats to bf16 (nearest, ties to even) and pack lo | hi << 16.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ void set_status(int32_t* status, int bits) {
+  if (status) atomicOr(status, bits);
+}
+
+}  // namespace skv

@@ -1,0 +1,26 @@
+// Host-side launchers of the libskv kernels (internal to the library).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace skv {
+
+cudaError_t launch_write_rows(const Geom& g, void* k, void* vt, const void* k_src,
+                              const void* v_src, int n_group, int n_tok, int mode, int row0,
+                              int32_t* head, int32_t* sync, const int32_t* tail_len,
+                              int32_t* status, cudaStream_t st);
+
+cudaError_t launch_rope_table(float* tab, int n_pos, int d, double theta, cudaStream_t st);
+
+cudaError_t launch_accept(int C, int blk, const int32_t* target, const int32_t* draft,
+                          int32_t* accept_len, int32_t* next_token, cudaStream_t st);
+
+cudaError_t launch_attn_simple(const Geom& g, int Hq, int mode, int n_tok, const void* q,
+                               void* out, float* lse, const int32_t* tail_len, const void* k,
+                               const void* vt, const float* rope, const int32_t* head,
+                               float sm_scale, int32_t* status, cudaStream_t st);
+
+}  // namespace skv

@@ -1,0 +1,113 @@
+"""The C ABI on a machine without a GPU: the library builds, loads and exports
+every declared symbol, and the host-side argument checks answer before any
+device work is enqueued."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from streaming_kv_cache_gb300 import build as B
+from streaming_kv_cache_gb300 import skv
+
+HEADER = os.path.join(B.ROOT, "include", "skv.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    B.build()
+    return skv.lib()
+
+
+def _declared():
+    src = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\*?\s+\*?([a-z_0-9]+)\(", src, flags=re.M)))
+
+
+def test_header_declares_the_binding_exports():
+    assert sorted(skv.EXPORTS) == _declared()
+
+
+def test_library_exports_every_declared_symbol(L):
+    out = subprocess.run(["nm", "-D", "--defined-only", B.LIB], capture_output=True, text=True).stdout
+    syms = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    for name in _declared():
+        assert name in syms, name
+        assert getattr(L, name) is not None
+
+
+def test_version_and_strings(L):
+    assert L.skv_version() == 1
+    for code in (0, -1, -2, -3, 1, 2, 4, 8, 6):
+        assert len(skv.status_string(code)) > 0
+
+
+def test_row_cap(L):
+    assert skv.skv_row_cap(256, 4, 4, 180, 128) == 3328
+    assert skv.skv_row_cap(512, 6, 8, 256, 128) == 12928
+    assert skv.skv_row_cap(8, 2, 2, 16, 32) == 128
+    assert L.skv_row_cap(-1, 1, 1, 1, 0) == -1
+    assert L.skv_row_cap(0, 0, 1, 1, 0) == -1
+
+
+FAKE = 0x10000  # never dereferenced: every case below fails validation first
+
+
+def _desc(**kw):
+    base = dict(n_cache=2, n_view=4, n_frame=4, frame_len=180, prefix_len=256, tail_cap=128,
+                n_kv_head=8, head_dim=128, row_cap=3328, rope_len=3264, k=FAKE, vt=FAKE * 2,
+                head=FAKE * 3, sync=FAKE * 4, rope=FAKE * 5, status=FAKE * 6, wait_ns=0)
+    base.update(kw)
+    return skv.skv_cache(**base)
+
+
+@pytest.mark.parametrize("bad", [
+    dict(head_dim=96), dict(head_dim=0), dict(n_view=0), dict(n_frame=0), dict(frame_len=0),
+    dict(prefix_len=-1), dict(tail_cap=-1), dict(n_kv_head=0), dict(row_cap=3200),
+    dict(row_cap=3330), dict(rope_len=3000), dict(k=0), dict(vt=0), dict(head=0), dict(sync=0),
+    dict(rope=0), dict(status=0), dict(k=FAKE + 8), dict(vt=FAKE + 2), dict(head=FAKE + 2),
+])
+def test_bad_cache_descriptor_is_rejected(L, bad):
+    d = _desc(**bad)
+    p = ctypes.c_void_p
+    assert L.kv_stream_insert(ctypes.byref(d), p(FAKE), p(FAKE), None) == skv.SKV_ERR_INVALID
+    assert L.stream_attn_prefill(ctypes.byref(d), 32, p(FAKE), p(FAKE), None, 1.0, None) == skv.SKV_ERR_INVALID
+
+
+def test_null_descriptor(L):
+    assert L.kv_stream_insert(None, None, None, None) == skv.SKV_ERR_INVALID
+    assert L.skv_verify_workspace_bytes(None, 32, 9) == 0
+
+
+def test_call_arguments_are_checked(L):
+    d = _desc()
+    p = ctypes.c_void_p
+    r = ctypes.byref(d)
+    # misaligned / null tensors
+    assert L.kv_stream_insert(r, p(FAKE + 4), p(FAKE), None) == skv.SKV_ERR_INVALID
+    assert L.kv_stream_insert(r, None, p(FAKE), None) == skv.SKV_ERR_INVALID
+    # query heads not a multiple of kv heads; group size not dividing 128
+    assert L.stream_attn_prefill(r, 30, p(FAKE), p(FAKE), None, 1.0, None) == skv.SKV_ERR_INVALID
+    assert L.stream_attn_prefill(r, 24, p(FAKE), p(FAKE), None, 1.0, None) == skv.SKV_ERR_UNSUPPORTED
+    assert L.stream_attn_prefill(r, 32, p(FAKE), p(FAKE), None, 0.0, None) == skv.SKV_ERR_INVALID
+    assert L.stream_attn_prefill(r, 32, p(FAKE), p(FAKE), p(FAKE + 2), 1.0, None) == skv.SKV_ERR_INVALID
+    # rows outside the cache
+    assert L.kv_write_rows(r, 3300, 29, p(FAKE), p(FAKE), None) == skv.SKV_ERR_INVALID
+    assert L.kv_write_rows(r, -1, 2, p(FAKE), p(FAKE), None) == skv.SKV_ERR_INVALID
+    ws = L.skv_verify_workspace_bytes(r, 32, 9)
+    args = [p(FAKE)] * 5
+    # block too large for the tail, or for 128 rows per kv head; ids half given
+    assert L.stream_attn_verify(r, 32, 129, *args, None, None, None, None, p(FAKE), ws, 1.0, None) == skv.SKV_ERR_INVALID
+    assert L.stream_attn_verify(r, 32, 33, *args, None, None, None, None, p(FAKE), ws, 1.0, None) == skv.SKV_ERR_UNSUPPORTED
+    assert L.stream_attn_verify(r, 32, 9, *args, p(FAKE), p(FAKE), None, p(FAKE), p(FAKE), ws, 1.0, None) == skv.SKV_ERR_INVALID
+    assert L.stream_attn_verify(r, 32, 0, *args, None, None, None, None, p(FAKE), ws, 1.0, None) == skv.SKV_ERR_INVALID
+
+
+def test_rope_table_arguments(L):
+    p = ctypes.c_void_p
+    assert L.skv_build_rope_table(None, 10, 128, 1e4, None) == skv.SKV_ERR_INVALID
+    assert L.skv_build_rope_table(p(FAKE), 0, 128, 1e4, None) == skv.SKV_ERR_INVALID
+    assert L.skv_build_rope_table(p(FAKE), 10, 127, 1e4, None) == skv.SKV_ERR_INVALID
+    assert L.skv_build_rope_table(p(FAKE), 10, 128, -1.0, None) == skv.SKV_ERR_INVALID
+    assert L.skv_build_rope_table(p(FAKE + 4), 10, 128, 1e4, None) == skv.SKV_ERR_INVALID

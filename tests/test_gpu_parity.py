@@ -1,0 +1,228 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle on the
+same seeded inputs.  Ring heads, cache bytes and accept lengths are compared
+bit for bit; attention outputs within max-abs 1e-2 and mean-abs 1e-3."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import skv_oracle as O
+from streaming_kv_cache_gb300 import skv, synth
+
+from gpu_harness import Pair, assert_close, bf16_dev_to_f64, from_dev, to_dev
+
+pytestmark = pytest.mark.gpu
+
+W = synth.WORKLOADS
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from streaming_kv_cache_gb300 import build
+    build.build()
+
+
+def _prefill_check(pair, step_tag, rows=None, watch=None, lse_tol=2e-3, rel=0.0):
+    w = pair.w
+    q = synth.frame_q(w, pair.n_inserts - 1, pair.tag + step_tag)
+    out, lse = skv.stream_attn_prefill(pair.cache, to_dev(q), w.sm_scale, lse=True)
+    got = bf16_dev_to_f64(out)
+    got_lse = lse.cpu().numpy()
+    for c in (pair.watch if watch is None else watch):
+        want, wl = O.stream_prefill(pair.win[c], q[c], w.theta, w.sm_scale, rows=rows)
+        sel = slice(None) if rows is None else rows
+        assert_close(got[c][sel], want, "%s cache %d" % (w.name, c), rel=rel)
+        err = np.abs(got_lse[c][:, sel].T - wl).max()
+        assert err < lse_tol, "lse err %g" % err
+    assert pair.cache.device_status() == 0
+    return got
+
+
+def test_insert_and_prefill_tiny():
+    pair = Pair(W["tiny"], "t0")
+    pair.fill()
+    pair.check_ring()
+    for s in range(W["tiny"].steps):
+        pair.insert()
+        pair.check_ring()
+        _prefill_check(pair, "s%d" % s)
+
+
+def test_prefill_alpamayo_step():
+    pair = Pair(W["alpamayo_step"], "a0")
+    pair.fill()
+    pair.insert()
+    pair.check_ring()
+    _prefill_check(pair, "x")
+
+
+def test_alpamayo_20_streaming_steps():
+    """Ring wraps 5 times; positions shift each step; every step's cache and
+    outputs against a full-window recompute."""
+    w = W["alpamayo_20steps"]
+    pair = Pair(w, "s20")
+    pair.fill()
+    for s in range(w.steps):
+        pair.insert()
+        pair.check_ring()
+        _prefill_check(pair, "s%d" % s)
+
+
+def test_prefill_scaleup_36_layers_sampled():
+    w = W["scaleup_36L"]
+    watch = [0, 17, 35]
+    pair = Pair(w, "big", watch=watch)
+    pair.fill()
+    pair.insert()
+    pair.check_ring()
+    rng = np.random.default_rng(5)
+    rows = sorted(set([0, 1, w.T - 1, w.T, 2 * w.T + 7, w.n_new - 1]
+                      + list(rng.integers(0, w.n_new, 26))))
+    _prefill_check(pair, "x", rows=np.array(rows), watch=watch)
+
+
+def test_prefill_peaky_queries():
+    """Q x 4: sharper softmax, larger logits.  Outputs then reach |o| > 4,
+    where rounding to bf16 alone costs up to 2^-8 |o|; that bound is added
+    to the absolute one."""
+    w = W["alpamayo_step"].with_(q_scale=4.0 / np.sqrt(128), C=2)
+    pair = Pair(w, "peak")
+    pair.fill()
+    pair.insert()
+    _prefill_check(pair, "x", rel=2.0 ** -8)
+
+
+@pytest.mark.parametrize("B", synth.VERIFY_BATCHES)
+def test_verify_alpamayo_batches(B):
+    w = W["alpamayo_verify"].with_(C=B)
+    pair = Pair(w, "v%d" % B)
+    pair.fill()
+    pair.insert()
+    pair.set_tail(w.tail_len)
+    q, k, v = synth.verify_block(w, pair.tag)
+    target, draft, planted = synth.planted_ids(B, w.blk, pair.tag)
+    tail = torch.full((B,), w.tail_len, dtype=torch.int32, device="cuda")
+    out, acc, nxt = skv.stream_attn_verify(
+        pair.cache, tail, to_dev(q), to_dev(k), to_dev(v), w.sm_scale,
+        target_ids=torch.from_numpy(target).cuda(), draft_ids=torch.from_numpy(draft).cuda())
+    got = bf16_dev_to_f64(out)
+    acc, nxt = acc.cpu().numpy(), nxt.cpu().numpy()
+    kk = from_dev(pair.cache.k)
+    vt = from_dev(pair.cache.vt)
+    base = pair.cache.n_visual + w.tail_len
+    for c in range(B):
+        want, _ = O.stream_verify(pair.win[c], q[c], k[c], v[c], w.theta, w.sm_scale)
+        assert_close(got[c], want, "verify B=%d cache %d" % (B, c))
+        a, n = O.accept_length(target[c], draft[c])
+        assert acc[c] == a == planted[c] and nxt[c] == n
+        # the block's K/V landed in the tail rows, bit-exact
+        np.testing.assert_array_equal(kk[c][:, base:base + w.blk].transpose(1, 0, 2), k[c])
+        np.testing.assert_array_equal(vt[c][:, :, base:base + w.blk].transpose(2, 0, 1), v[c])
+    assert pair.cache.device_status() == 0
+
+
+def test_verify_tiny_and_tail_advance():
+    """Two verify rounds; the caller advances tail_len by accept_len + 1."""
+    w = W["tiny"].with_(C=3, blk=9)
+    pair = Pair(w, "vt")
+    pair.fill()
+    tail = torch.zeros((w.C,), dtype=torch.int32, device="cuda")
+    tail_host = np.zeros(w.C, np.int64)
+    tk = {c: np.zeros((0, w.Hkv, w.d), np.uint16) for c in range(w.C)}
+    tv = {c: np.zeros((0, w.Hkv, w.d), np.uint16) for c in range(w.C)}
+    for rnd in range(2):
+        q, k, v = synth.verify_block(w, "r%d" % rnd)
+        target, draft, _ = synth.planted_ids(w.C, w.blk, "r%d" % rnd)
+        out, acc, nxt = skv.stream_attn_verify(
+            pair.cache, tail, to_dev(q), to_dev(k), to_dev(v), w.sm_scale,
+            target_ids=torch.from_numpy(target).cuda(), draft_ids=torch.from_numpy(draft).cuda())
+        got = bf16_dev_to_f64(out)
+        acc_h = acc.cpu().numpy()
+        for c in range(w.C):
+            pair.win[c].set_tail(tk[c], tv[c])
+            want, _ = O.stream_verify(pair.win[c], q[c], k[c], v[c], w.theta, w.sm_scale)
+            assert_close(got[c], want, "tiny verify round %d cache %d" % (rnd, c))
+            keep = int(acc_h[c]) + 1
+            tk[c] = np.concatenate([tk[c], k[c][:keep]])
+            tv[c] = np.concatenate([tv[c], v[c][:keep]])
+            tail_host[c] += keep
+        tail += acc + 1
+        np.testing.assert_array_equal(tail.cpu().numpy(), tail_host)
+
+
+def test_verify_tail_overflow_sets_status():
+    w = W["tiny"].with_(C=2, blk=9)
+    pair = Pair(w, "ovf")
+    pair.fill()
+    before_k = from_dev(pair.cache.k)
+    tail = torch.tensor([w.tail_cap - 8, 0], dtype=torch.int32, device="cuda")
+    q, k, v = synth.verify_block(w, "ovf")
+    out = torch.zeros((w.C, w.blk, w.Hq, w.d), dtype=torch.bfloat16, device="cuda")
+    skv.stream_attn_verify(pair.cache, tail, to_dev(q), to_dev(k), to_dev(v), w.sm_scale, out=out)
+    assert pair.cache.device_status() & skv.SKV_DEV_TAIL_OVERFLOW
+    after_k = from_dev(pair.cache.k)
+    np.testing.assert_array_equal(after_k[0], before_k[0])      # cache 0 skipped entirely
+    assert (from_dev(out)[0] == 0).all()
+    want, _ = O.stream_verify(pair.win[1], q[1], k[1], v[1], w.theta, w.sm_scale)
+    assert_close(bf16_dev_to_f64(out)[1], want, "cache 1 unaffected")
+
+
+def test_bad_head_sets_status():
+    w = W["tiny"].with_(C=2)
+    pair = Pair(w, "bh")
+    pair.fill()
+    pair.cache.head[1, 0] = w.F + 3
+    k, v = synth.frame_kv(w, 99, "bh")
+    skv.kv_stream_insert(pair.cache, to_dev(k), to_dev(v))
+    assert pair.cache.device_status() & skv.SKV_DEV_BAD_HEAD
+    heads = pair.cache.head.cpu().numpy()
+    assert heads[1, 0] == w.F + 3 and (heads[0] == 1).all() and heads[1, 1] == 1
+
+
+def test_untouched_rows_keep_their_bytes():
+    """Finite poison in the tail and padding rows survives inserts."""
+    w = W["alpamayo_step"].with_(C=2)
+    pair = Pair(w, "poison")
+    nv = pair.cache.n_visual
+    pair.cache.k[:, :, nv:] = 1536.0
+    pair.cache.vt[:, :, :, nv:] = -77.0
+    pair.fill()
+    pair.insert()
+    pair.insert()
+    pair.check_ring()
+    assert (pair.cache.k[:, :, nv:] == 1536.0).all()
+    assert (pair.cache.vt[:, :, :, nv:] == -77.0).all()
+    _prefill_check(pair, "p")
+
+
+def test_checkpoint_resume_mid_stream():
+    """Copy the cache state to the host mid-stream, restore it into a fresh
+    cache, and continue: identical bytes and outputs."""
+    w = W["tiny"].with_(C=2)
+    a = Pair(w, "ckpt")
+    a.fill()
+    a.insert()
+    saved = {n: getattr(a.cache, n).cpu() for n in ("k", "vt", "head", "sync")}
+    b = skv.StreamCache(w.C, w.P, w.V, w.F, w.T, w.Hkv, w.d, w.theta, tail_cap=w.tail_cap)
+    for n, t in saved.items():
+        getattr(b, n).copy_(t)
+    k, v = synth.frame_kv(w, a.n_inserts, a.tag)
+    q = synth.frame_q(w, a.n_inserts, a.tag)
+    a.insert()
+    skv.kv_stream_insert(b, to_dev(k), to_dev(v))
+    oa = skv.stream_attn_prefill(a.cache, to_dev(q), w.sm_scale)
+    ob = skv.stream_attn_prefill(b, to_dev(q), w.sm_scale)
+    assert torch.equal(a.cache.k, b.k) and torch.equal(a.cache.vt, b.vt)
+    assert torch.equal(a.cache.head, b.head)
+    assert torch.equal(oa, ob)
+
+
+def test_empty_cache_set_is_a_no_op():
+    w = W["tiny"].with_(C=0)
+    cache = skv.StreamCache(0, w.P, w.V, w.F, w.T, w.Hkv, w.d, w.theta, tail_cap=w.tail_cap)
+    e = torch.empty((0, w.V, w.T, w.Hkv, w.d), dtype=torch.bfloat16, device="cuda")
+    skv.kv_stream_insert(cache, e, e)
+    q = torch.empty((0, w.n_new, w.Hq, w.d), dtype=torch.bfloat16, device="cuda")
+    out = skv.stream_attn_prefill(cache, q, w.sm_scale)
+    assert out.numel() == 0
