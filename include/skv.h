@@ -48,6 +48,7 @@ extern "C" {
 #define SKV_ERR_INVALID (-1)     /* null/misaligned pointer, bad shape or argument */
 #define SKV_ERR_UNSUPPORTED (-2) /* no sm_103 device current, or shape outside what the kernels cover */
 #define SKV_ERR_CUDA (-3)        /* a CUDA runtime/driver call failed; see skv_last_cuda_error() */
+#define SKV_ERR_TOO_LARGE (-4)   /* shape exceeds the fixed scratch of kv_stream_insert_noalloc */
 
 /* device status bits (OR-ed into *cache->status) */
 #define SKV_DEV_TIMEOUT 1        /* a bounded wait inside a kernel gave up; outputs are undefined */
@@ -150,6 +151,35 @@ int kv_write_rows(const skv_cache* cache, int32_t row0, int32_t n_rows, const vo
  */
 int kv_stream_insert(const skv_cache* cache, const void* k_new, const void* v_new,
                      void* stream);
+
+/*
+ * kv_stream_insert_noalloc -- kv_stream_insert for callers that cannot
+ * allocate device memory.  Some callers of this library may not call
+ * cudaMalloc at all: an inference runtime that hands its plug-ins only the
+ * buffers it planned ahead of time, a real-time control loop that must
+ * never block in the allocator, or code running where allocation is
+ * forbidden after start-up.  Such a caller cannot provide the scratch
+ * counters kv_stream_insert needs in cache->sync.  The pages have no
+ * counterpart to this call; it only changes where that scratch lives.
+ *
+ * Same inputs, outputs and results as kv_stream_insert; cache->sync is
+ * ignored and may be NULL.  The per-(cache, view) arrival counters live in
+ * one file-scope static device array of SKV_NOALLOC_MAX_CACHE_VIEWS int32
+ * (64 KiB), which every GPU that loads libskv holds until the process
+ * exits.  n_cache * n_view above that limit returns SKV_ERR_TOO_LARGE and
+ * enqueues nothing.
+ *
+ * The first call on a device looks up the array's device address, with
+ * that device current; make that first call before any stream capture.
+ * Every call first clears the counters it uses with an asynchronous memset
+ * on `stream`; it calls no cudaMalloc, cudaFree or allocating library
+ * routine.  All calls on one device share the one array and it keeps what
+ * the last call left, so calls that overlap on that GPU (for instance on
+ * two streams) race: serialise them.
+ */
+#define SKV_NOALLOC_MAX_CACHE_VIEWS 16384
+int kv_stream_insert_noalloc(const skv_cache* cache, const void* k_new, const void* v_new,
+                             void* stream);
 
 /*
  * stream_attn_prefill -- attention of the newest frame's tokens over the

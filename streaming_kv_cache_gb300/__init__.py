@@ -5,6 +5,7 @@ kv_stream_insert, stream_attn_prefill and stream_attn_verify, plus a thin
 ctypes binding.  Build it with streaming_kv_cache_gb300.build.build().
 """
 from . import synth  # noqa: F401
-from .skv import (EXPORTS, SkvError, StreamCache, kv_stream_insert, kv_write_rows,  # noqa: F401
+from .skv import (EXPORTS, SkvError, StreamCache, kv_stream_insert,  # noqa: F401
+                  kv_stream_insert_noalloc, kv_write_rows,
                   lib, skv_build_rope_table, skv_row_cap, skv_verify_workspace_bytes,
                   status_string, stream_attn_prefill, stream_attn_verify, verify_workspace)

@@ -58,6 +58,22 @@ int check_cache(const skv_cache* c) {
 
 }  // namespace
 
+namespace skv {
+
+// The argument checks kv_stream_insert makes, without enqueueing anything;
+// lets a caller validate before it enqueues work of its own.
+int check_insert_args(const skv_cache* cache, const void* k_new, const void* v_new) {
+  int rc = check_cache(cache);
+  if (rc) return rc;
+  if (cache->n_cache == 0) return SKV_OK;
+  if (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new)) return SKV_ERR_INVALID;
+  return check_device();
+}
+
+int record_cuda_error(cudaError_t e) { return cuda_fail(e); }
+
+}  // namespace skv
+
 extern "C" {
 
 int skv_version(void) { return SKV_VERSION; }
@@ -68,6 +84,7 @@ const char* skv_status_string(int code) {
     case SKV_ERR_INVALID: return "invalid argument (null/misaligned pointer or bad shape)";
     case SKV_ERR_UNSUPPORTED: return "unsupported (no sm_103 device current, or shape outside the kernels)";
     case SKV_ERR_CUDA: return "CUDA call failed (see skv_last_cuda_error)";
+    case SKV_ERR_TOO_LARGE: return "n_cache * n_view exceeds the static scratch of kv_stream_insert_noalloc";
     case SKV_DEV_TIMEOUT: return "device: a bounded wait gave up";
     case SKV_DEV_BAD_HEAD: return "device: ring head outside [0, F)";
     case SKV_DEV_TAIL_OVERFLOW: return "device: tail_len + blk exceeds tail_cap";

@@ -14,12 +14,14 @@ import torch
 
 _LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libskv.so")
 
-SKV_OK, SKV_ERR_INVALID, SKV_ERR_UNSUPPORTED, SKV_ERR_CUDA = 0, -1, -2, -3
+SKV_OK, SKV_ERR_INVALID, SKV_ERR_UNSUPPORTED, SKV_ERR_CUDA, SKV_ERR_TOO_LARGE = 0, -1, -2, -3, -4
+SKV_NOALLOC_MAX_CACHE_VIEWS = 16384
 SKV_DEV_TIMEOUT, SKV_DEV_BAD_HEAD, SKV_DEV_TAIL_OVERFLOW, SKV_DEV_BAD_TAIL = 1, 2, 4, 8
 
 # every function the C header declares
 EXPORTS = ("skv_version", "skv_status_string", "skv_last_cuda_error", "skv_row_cap",
-           "skv_build_rope_table", "kv_write_rows", "kv_stream_insert", "stream_attn_prefill",
+           "skv_build_rope_table", "kv_write_rows", "kv_stream_insert", "kv_stream_insert_noalloc",
+           "stream_attn_prefill",
            "skv_verify_workspace_bytes", "stream_attn_verify")
 
 
@@ -65,6 +67,7 @@ def lib():
             "skv_build_rope_table": ([P, I32, I32, ctypes.c_double, P], ctypes.c_int),
             "kv_write_rows": ([cp, I32, I32, P, P, P], ctypes.c_int),
             "kv_stream_insert": ([cp, P, P, P], ctypes.c_int),
+            "kv_stream_insert_noalloc": ([cp, P, P, P], ctypes.c_int),
             "stream_attn_prefill": ([cp, I32, P, P, P, ctypes.c_float, P], ctypes.c_int),
             "skv_verify_workspace_bytes": ([cp, I32, I32], SZ),
             "stream_attn_verify": ([cp, I32, I32, P, P, P, P, P, P, P, P, P, P, SZ,
@@ -180,6 +183,19 @@ def kv_stream_insert(cache: StreamCache, k_new: torch.Tensor, v_new: torch.Tenso
     d = cache.desc()
     _check(lib().kv_stream_insert(ctypes.byref(d), _ptr(k_new), _ptr(v_new), _stream()),
            "kv_stream_insert")
+
+
+def kv_stream_insert_noalloc(cache: StreamCache, k_new: torch.Tensor, v_new: torch.Tensor):
+    """kv_stream_insert without caller scratch: for callers that may not
+    allocate device memory, the insert's counters live in a fixed static
+    device array inside the library (cache.sync is not used)."""
+    shp = (cache.C, cache.V, cache.T, cache.Hkv, cache.d)
+    _need(k_new, shp, torch.bfloat16, "k_new")
+    _need(v_new, shp, torch.bfloat16, "v_new")
+    d = cache.desc()
+    d.sync = None
+    _check(lib().kv_stream_insert_noalloc(ctypes.byref(d), _ptr(k_new), _ptr(v_new), _stream()),
+           "kv_stream_insert_noalloc")
 
 
 def stream_attn_prefill(cache: StreamCache, q_new: torch.Tensor, sm_scale: float,
