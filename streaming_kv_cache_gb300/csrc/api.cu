@@ -151,9 +151,9 @@ int stream_attn_prefill(const skv_cache* cache, int32_t n_q_head, const void* q_
   if (lse && ((uintptr_t)lse & 3u)) return SKV_ERR_INVALID;
   if ((rc = check_device())) return rc;
   const skv::Geom g = skv::geom_of(*cache);
-  cudaError_t e = skv::launch_attn_simple(g, n_q_head, 0, g.V * g.T, q_new, out, lse, nullptr,
-                                          cache->k, cache->vt, cache->rope, cache->head, sm_scale,
-                                          cache->status, (cudaStream_t)stream);
+  cudaError_t e = skv::launch_prefill_tc(g, n_q_head, q_new, out, lse, cache->k, cache->vt, cache->rope,
+                                         cache->head, sm_scale, cache->status, cache->wait_ns,
+                                         (cudaStream_t)stream);
   return e == cudaSuccess ? SKV_OK : cuda_fail(e);
 }
 

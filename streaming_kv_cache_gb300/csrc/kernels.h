@@ -23,6 +23,10 @@ cudaError_t launch_attn_simple(const Geom& g, int Hq, int mode, int n_tok, const
                                const void* vt, const float* rope, const int32_t* head,
                                float sm_scale, int32_t* status, cudaStream_t st);
 
+cudaError_t launch_prefill_tc(const Geom& g, int Hq, const void* q, void* out, float* lse, const void* k,
+                              const void* vt, const float* rope, const int32_t* head, float sm_scale,
+                              int32_t* status, uint64_t wait_ns, cudaStream_t st);
+
 int check_insert_args(const skv_cache* cache, const void* k_new, const void* v_new);
 int record_cuda_error(cudaError_t e);
 

@@ -54,8 +54,9 @@ class Pair:
         self.win = {c: O.StreamWindow(w.P, w.V, w.F, w.T, w.Hkv, w.d, pk[c], pv[c]) for c in self.watch}
         self.n_inserts = 0
 
-    def insert(self):
-        k, v = synth.frame_kv(self.w, self.n_inserts, self.tag)
+    def insert(self, k=None, v=None):
+        if k is None:
+            k, v = synth.frame_kv(self.w, self.n_inserts, self.tag)
         skv.kv_stream_insert(self.cache, to_dev(k), to_dev(v))
         for c, win in self.win.items():
             win.insert(k[c], v[c])
