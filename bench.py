@@ -217,6 +217,67 @@ def run_reference(args, rank, world):
                   "d2h_bytes_per_step": 0}})
 
 
+def run_only(args):
+    """One kernel alone on a reduced case (for ncu captures): scale-up
+    geometry with --layers caches for prefill/insert, the verify workload
+    with batch --layers for verify."""
+    import torch
+    from streaming_kv_cache_gb300 import build as B
+    B.build()
+    from streaming_kv_cache_gb300 import skv
+    dev = torch.device("cuda", 0)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(7)
+
+    def randn(shape, scale=1.0):
+        return (torch.randn(shape, generator=gen, device=dev) * scale).to(torch.bfloat16)
+
+    w = (VERIFY_W if args.only == "verify" else PREFILL_W).with_(C=args.layers)
+    cache = skv.StreamCache(w.C, w.P, w.V, w.F, w.T, w.Hkv, w.d, w.theta, tail_cap=w.tail_cap)
+    skv.kv_write_rows(cache, 0, randn((w.C, w.P, w.Hkv, w.d)), randn((w.C, w.P, w.Hkv, w.d)))
+    k_new = randn((w.C, w.V, w.T, w.Hkv, w.d))
+    for _ in range(w.F):
+        skv.kv_stream_insert(cache, k_new, k_new)
+    if args.only == "prefill":
+        q = randn((w.C, w.n_new, w.Hq, w.d), w.q_scale)
+        out = torch.empty_like(q)
+        fn = lambda: skv.stream_attn_prefill(cache, q, w.sm_scale, out=out)
+        work = prefill_flop(w) / 1e12
+        unit = "TFLOP/s"
+    elif args.only == "insert":
+        fn = lambda: skv.kv_stream_insert(cache, k_new, k_new)
+        work = insert_bytes(w) / 1e9
+        unit = "GB/s"
+    else:
+        skv.kv_write_rows(cache, cache.n_visual, randn((w.C, w.tail_len, w.Hkv, w.d)),
+                          randn((w.C, w.tail_len, w.Hkv, w.d)))
+        qb = randn((w.C, w.blk, w.Hq, w.d), w.q_scale)
+        kb = randn((w.C, w.blk, w.Hkv, w.d))
+        tail = torch.full((w.C,), w.tail_len, dtype=torch.int32, device=dev)
+        ws = skv.verify_workspace(cache, w.Hq, w.blk)
+        out = torch.empty_like(qb)
+        fn = lambda: skv.stream_attn_verify(cache, tail, qb, kb, kb, w.sm_scale, ws=ws, out=out)
+        work = verify_bytes(w) / 1e9
+        unit = "GB/s"
+    for _ in range(args.warmup):
+        fn()
+    torch.cuda.synchronize()
+    ms = []
+    for _ in range(args.steps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        torch.cuda.synchronize()
+        ms.append(a.elapsed_time(b))
+    status = cache.device_status()
+    med = statistics.median(ms)
+    emit({"only": args.only, "layers_or_batch": w.C, "ms_median": med, "ms": ms,
+          "throughput": work / (med * 1e-3), "unit": unit, "device_status": status})
+    if status:
+        sys.exit(3)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -224,6 +285,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", choices=["prefill", "verify", "insert"], default=None,
+                    help="profiling aid: time one kernel alone on a reduced case and print its ms")
+    ap.add_argument("--layers", type=int, default=4,
+                    help="layer caches (prefill/insert) or batch (verify) of the --only case")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -234,6 +299,9 @@ def main():
 
     if args.impl == "reference":
         run_reference(args, rank, world)
+        return
+    if args.only:
+        run_only(args)
         return
 
     import torch

@@ -17,8 +17,11 @@
 //   warp  8     TMA producer (K tile, V^T tile) and TMEM allocator
 //   warp  9     MMA issuer: S_i = Q_i K^T (smem x smem, fp16 rotated
 //               operands), O_i += P_i V (bf16 P from TMEM, bf16 V^T from smem)
-//   warps 10-13 RoPE: rotate Q once, then every K tile in shared memory
+//   warps 10-11 idle (complete the third warpgroup)
+//   warps 12-15 RoPE: rotate Q once, then every K tile in shared memory
 //               between the TMA landing and the MMA
+// Registers are re-split per warpgroup with setmaxnreg: the softmax threads
+// hold a whole 128-score row (192 registers), the others shrink.
 //
 // TMEM (512 columns): S0 [0,128) S1 [128,256) O0 [256,256+D) O1 [384,384+D);
 // P_i (bf16 pairs) overwrites the first 64 columns of S_i.
@@ -38,9 +41,13 @@ namespace {
 constexpr int BM = 128;          // rows per query tile
 constexpr int BN = 128;          // keys per tile
 constexpr int NSTAGE = 2;
-constexpr int NTHREADS = 448;
-constexpr int WARP_TMA = 8, WARP_MMA = 9, WARP_ROPE = 10;
+constexpr int NTHREADS = 512;
+constexpr int WARP_TMA = 8, WARP_MMA = 9, WARP_ROPE = 12;
+// register split (launch: 512 threads x 128): 2 x 128 x 176 + 128 x 56 + 128 x 104 = 65536
+constexpr int REG_SOFTMAX = 176, REG_CTRL = 56, REG_ROPE = 104;
+static_assert(256 * REG_SOFTMAX + 128 * REG_CTRL + 128 * REG_ROPE == 65536, "register split");
 constexpr int MAX_TILES = 1024;
+constexpr int MAX_VIEWS = 64;
 constexpr float RESCALE_THRESHOLD = 8.0f;
 constexpr uint64_t DRAIN_NS = 500000000ull;  // bounded wait for own in-flight copies/MMAs
 
@@ -57,7 +64,8 @@ struct Layout {
   static constexpr int BAR_OFF = V_OFF + NSTAGE * VT;
   static constexpr int NBAR = 18;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
-  static constexpr int TILE_OFF = MISC_OFF + 64;
+  static constexpr int HEAD_OFF = MISC_OFF + 64;     // ring heads of this cache (<= MAX_VIEWS)
+  static constexpr int TILE_OFF = HEAD_OFF + MAX_VIEWS * 4;
   static constexpr int BYTES = TILE_OFF + MAX_TILES * 4;
   static constexpr int ALLOC = BYTES + 1024;   // slack for 1024-byte alignment
 };
@@ -86,17 +94,60 @@ struct PrefillParams {
 // b their partners x_{e+d/2}..; cs[k] = (cos, sin) of element e+k.  The rotated
 // Q and K feed an fp16 x fp16 tensor-core product (3 more significand bits
 // than bf16); values are clamped to the finite fp16 range.
-__device__ __forceinline__ void rotate_pairs(uint4& a, uint4& b, const float2* __restrict__ cs) {
+// t[w] = (cos, sin) of elements 2w and 2w+1 of the chunk.
+__device__ __forceinline__ void rotate_pairs4(uint4& a, uint4& b, const float4 (&t)[4]) {
   uint32_t* pa = reinterpret_cast<uint32_t*>(&a);
   uint32_t* pb = reinterpret_cast<uint32_t*>(&b);
-  const float4* c4 = reinterpret_cast<const float4*>(cs);
 #pragma unroll
   for (int w = 0; w < 4; ++w) {
-    const float4 t = __ldg(c4 + w);   // (cos, sin) of elements 2w and 2w+1
     const float x0 = bf16_lo(pa[w]), x1 = bf16_hi(pa[w]);
     const float y0 = bf16_lo(pb[w]), y1 = bf16_hi(pb[w]);
-    pa[w] = pack_f16x2_sat(x0 * t.x - y0 * t.y, x1 * t.z - y1 * t.w);
-    pb[w] = pack_f16x2_sat(y0 * t.x + x0 * t.y, y1 * t.z + x1 * t.w);
+    pa[w] = pack_f16x2_sat(x0 * t[w].x - y0 * t[w].y, x1 * t[w].z - y1 * t[w].w);
+    pb[w] = pack_f16x2_sat(y0 * t[w].x + x0 * t[w].y, y1 * t[w].z + x1 * t[w].w);
+  }
+}
+
+__device__ __forceinline__ void rotate_pairs(uint4& a, uint4& b, const float2* __restrict__ cs) {
+  const float4* c4 = reinterpret_cast<const float4*>(cs);
+  float4 t[4];
+#pragma unroll
+  for (int w = 0; w < 4; ++w) t[w] = __ldg(c4 + w);
+  rotate_pairs4(a, b, t);
+}
+
+// Logical position of physical key row r and how many rows from r on (r
+// included) continue with consecutive positions: the rest of the prefix, of
+// the ring frame, or the tail.
+__device__ __forceinline__ void key_pos_run(const Geom& g, const int* __restrict__ heads, int r, int& pos,
+                                            int& run) {
+  const int u = r - g.P;
+  if (u < 0) {
+    pos = r;
+    run = g.P - r;
+    return;
+  }
+  if (u >= g.ring_rows()) {
+    pos = r;
+    run = 1 << 30;
+    return;
+  }
+  const int FT = g.F * g.T;
+  const int v = u / FT;
+  const int rem = u - v * FT;
+  const int sl = rem / g.T;
+  const int t = rem - sl * g.T;
+  int f = sl - heads[v];
+  if (f < 0) f += g.F;
+  pos = g.P + v * FT + f * g.T + t;
+  run = g.T - t;
+}
+
+__device__ __forceinline__ void advance_angles(float4 (&cs)[4], const float4 (&st)[4]) {
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    const float4 c = cs[w];
+    cs[w] = make_float4(c.x * st[w].x - c.y * st[w].y, c.y * st[w].x + c.x * st[w].y,
+                        c.z * st[w].z - c.w * st[w].w, c.w * st[w].z + c.z * st[w].w);
   }
 }
 
@@ -113,6 +164,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + L::MISC_OFF + 4);
   int* s_ntiles = reinterpret_cast<int*>(smem + L::MISC_OFF + 8);
   int* s_tiles = reinterpret_cast<int*>(smem + L::TILE_OFF);
+  int* s_head = reinterpret_cast<int*>(smem + L::HEAD_OFF);
 
   const Geom& g = p.g;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -143,6 +195,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
     for (int v = 0; v <= vq; ++v) {
       const int hv = head_c[v];
       if (hv < 0 || hv >= g.F) ok = 0;
+      s_head[v] = hv;
     }
     int n = 0;
     if (ok) {
@@ -170,6 +223,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
   const uint32_t tmem = *s_tmem;
   const int nt = *s_ntiles;
 
+  if (warp >= 8 && warp < WARP_ROPE) {
+    tc::setmaxnreg_dec<REG_CTRL>();
   if (warp == WARP_TMA) {
     // ------------------------------------------------------------ producer
     if (lane == 0 && nt > 0) {
@@ -209,21 +264,25 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
     if (lane == 0 && nt > 0) {
       constexpr uint32_t idesc_qk = tc::idesc_f16(BM, BN);
       constexpr uint32_t idesc_pv = tc::idesc_bf16(BM, D);
+      // descriptors advance by adding (byte offset >> 4) to the start-address field
+      const uint64_t dq0 = tc::sdesc_sw128(sbase + L::Q_OFF);
+      const uint64_t dk0 = tc::sdesc_sw128(sbase + L::K_OFF);
+      const uint64_t dv0 = tc::sdesc_sw128(sbase + L::V_OFF);
       auto issue_qk = [&](int i, int s) {
-        const uint32_t qa = sbase + L::Q_OFF + i * L::QT;
-        const uint32_t kb = sbase + L::K_OFF + s * L::KT;
-#pragma unroll
+        const uint64_t dq = dq0 + ((uint32_t)(i * L::QT) >> 4);
+        const uint64_t dk = dk0 + ((uint32_t)(s * L::KT) >> 4);
+#pragma unroll 1
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * L::HALF_Q + (kk & 3) * 32;
-          tc::mma_ss(tmem + i * 128, tc::sdesc_sw128(qa + off), tc::sdesc_sw128(kb + off), idesc_qk, kk > 0);
+          const uint32_t off = ((kk >> 2) * L::HALF_Q + (kk & 3) * 32) >> 4;
+          tc::mma_ss(tmem + i * 128, dq + off, dk + off, idesc_qk, kk > 0);
         }
       };
       auto issue_pv = [&](int i, int s, bool acc) {
-        const uint32_t vb = sbase + L::V_OFF + s * L::VT;
-#pragma unroll
+        const uint64_t dv = dv0 + ((uint32_t)(s * L::VT) >> 4);
+#pragma unroll 1
         for (int kk = 0; kk < BN / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * L::HALF_V + (kk & 3) * 32;
-          tc::mma_ts(tmem + 256 + i * 128, tmem + i * 128 + kk * 8, tc::sdesc_sw128(vb + off), idesc_pv,
+          const uint32_t off = ((kk >> 2) * L::HALF_V + (kk & 3) * 32) >> 4;
+          tc::mma_ts(tmem + 256 + i * 128, tmem + i * 128 + kk * 8, dv + off, idesc_pv,
                      (acc || kk > 0) ? 1u : 0u);
         }
       };
@@ -268,8 +327,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
       volatile int never = 0;
       tc::mbar_wait(bar(B_DRAIN), 0, DRAIN_NS, &never);
     }
+  }
   } else if (warp >= WARP_ROPE) {
     // ----------------------------------------------------------------- RoPE
+    tc::setmaxnreg_dec<REG_ROPE>();
     const int rt = tid - WARP_ROPE * 32;   // 0..127: row of the tile
     constexpr int HALF = D / 2;
     // query tiles: rotate each row at its logical position and store it in
@@ -301,7 +362,35 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
     }
     tc::fence_proxy_async_smem();
     tc::mbar_arrive(bar(B_QFULL));
-    // key tiles: rotate in place once TMA has landed them
+    // key tiles, rotated in place once TMA has landed them.  Thread (warp wr,
+    // lane ln) takes chunk ch = ln % NCH (8 frequencies) of NCH consecutive
+    // rows; inside a frame consecutive rows have consecutive positions, so
+    // their (cos, sin) advance by one complex multiplication with R(1)
+    // instead of a table load.  The first row's table entries of the next
+    // tile are fetched while the current tile is rotated.
+    constexpr int NCH = HALF / 8;
+    const int wr = rt >> 5, ln = rt & 31;
+    const int ch = ln % NCH;
+    const int row_base = wr * 32 + (ln / NCH) * NCH;
+    const int ea = ch * 8, eb = HALF + ch * 8;
+    const uint32_t off_a = (ea / 64) * L::HALF_Q, off_b = (eb / 64) * L::HALF_Q;
+    const int ca = (ea % 64) / 8, cb = (eb % 64) / 8;
+    const float4* rope4 = reinterpret_cast<const float4*>(p.rope);
+    float4 step[4];
+#pragma unroll
+    for (int w4 = 0; w4 < 4; ++w4) step[w4] = __ldg(rope4 + (HALF + ea) / 2 + w4);   // R(1)
+    int pf_pos = -1, pf_run = 0;
+    float4 pf[4];
+    auto fetch = [&](int jj) {
+      const int r = s_tiles[jj] + row_base;
+      pf_pos = -1;
+      if (r < row_end) {
+        key_pos_run(g, s_head, r, pf_pos, pf_run);
+#pragma unroll
+        for (int w4 = 0; w4 < 4; ++w4) pf[w4] = __ldg(rope4 + ((size_t)pf_pos * HALF + ea) / 2 + w4);
+      }
+    };
+    if (nt > 0) fetch(0);
 #pragma unroll 1
     for (int j = 0; j < nt; ++j) {
       const int s = j & 1, u = j >> 1;
@@ -309,27 +398,42 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
         set_status(p.status, SKV_DEV_TIMEOUT);
         break;
       }
-      const int r = s_tiles[j] + rt;
-      if (r < row_end) {
-        const int pos = key_index(g, head_c, r);
-        const float2* cs = p.rope + (size_t)pos * HALF;
+      if (pf_pos >= 0) {
         uint8_t* kt = smem + L::K_OFF + s * L::KT;
+        const int r0 = s_tiles[j] + row_base;
+        int pos = pf_pos, run = pf_run;
+        float4 cs[4] = {pf[0], pf[1], pf[2], pf[3]};
 #pragma unroll
-        for (int ch = 0; ch < HALF / 8; ++ch) {
-          const int ea = ch * 8, eb = HALF + ch * 8;
-          uint4* pa = reinterpret_cast<uint4*>(kt + (ea / 64) * L::HALF_Q + tc::sw128_off(rt, (ea % 64) / 8));
-          uint4* pb = reinterpret_cast<uint4*>(kt + (eb / 64) * L::HALF_Q + tc::sw128_off(rt, (eb % 64) / 8));
-          uint4 a = *pa, b = *pb;
-          rotate_pairs(a, b, cs + ea);
-          *pa = a;
-          *pb = b;
+        for (int k = 0; k < NCH; ++k) {
+          const int r = r0 + k;
+          if (r >= row_end) break;
+          if (k > 0) {
+            if (run > 1) {
+              --run;
+              ++pos;
+              advance_angles(cs, step);
+            } else {
+              key_pos_run(g, s_head, r, pos, run);
+#pragma unroll
+              for (int w4 = 0; w4 < 4; ++w4) cs[w4] = __ldg(rope4 + ((size_t)pos * HALF + ea) / 2 + w4);
+            }
+          }
+          const int row = row_base + k;
+          uint4* pa = reinterpret_cast<uint4*>(kt + off_a + tc::sw128_off(row, ca));
+          uint4* pb = reinterpret_cast<uint4*>(kt + off_b + tc::sw128_off(row, cb));
+          uint4 xa = *pa, xb = *pb;
+          rotate_pairs4(xa, xb, cs);
+          *pa = xa;
+          *pb = xb;
         }
       }
+      if (j + 1 < nt) fetch(j + 1);
       tc::fence_proxy_async_smem();
       tc::mbar_arrive(bar(B_KROT + s));
     }
   } else {
     // ------------------------------------------------- softmax + epilogue
+    tc::setmaxnreg_inc<REG_SOFTMAX>();
     const int i = warp >> 2;            // query tile
     const int lg = warp & 3;            // TMEM lane group of this warp
     const int row = lg * 32 + lane;
@@ -354,24 +458,30 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
       ok = __all_sync(0xffffffffu, tc::mbar_wait(bar(B_SFULL + i), j & 1, wait_ns, s_abort));
       if (!ok) break;
       tc::tc_fence_after();
+      // the whole 128-score row in one TMEM round trip
+      uint32_t v[BN];
+#pragma unroll
+      for (int cb = 0; cb < BN / 32; ++cb)
+        tc::tmem_ld32(tS + cb * 32, *reinterpret_cast<uint32_t(*)[32]>(v + cb * 32));
       const int r0 = s_tiles[j];
       const int a = inv_a - r0, b = inv_b - r0, e = row_end - r0;
       const bool full = (a >= BN || b <= 0 || a >= b) && e >= BN;
-      const uint32_t span = (uint32_t)max(b - a, 0);
-      // pass 1: row max of the scaled scores
-      float mx = -INFINITY;
+      tc::tmem_wait_ld();
+      if (!__all_sync(0xffffffffu, full)) {
+        const uint32_t span = (uint32_t)max(b - a, 0);
 #pragma unroll
-      for (int cb = 0; cb < BN / 32; ++cb) {
-        uint32_t v[32];
-        tc::tmem_ld32(tS + cb * 32, v);
-        tc::tmem_wait_ld();
-#pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          const int kk = cb * 32 + k;
-          const bool vis = full || ((uint32_t)(kk - a) >= span && kk < e);
-          mx = fmaxf(mx, vis ? __uint_as_float(v[k]) * sl : -INFINITY);
-        }
+        for (int k = 0; k < BN; ++k)
+          if (!((uint32_t)(k - a) >= span && k < e)) v[k] = __float_as_uint(-INFINITY);
       }
+      // row max with 8 independent chains
+      float m8[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) m8[q] = __uint_as_float(v[q]);
+#pragma unroll
+      for (int k = 8; k < BN; ++k) m8[k & 7] = fmaxf(m8[k & 7], __uint_as_float(v[k]));
+      float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                       fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+      mx *= sl;
       const bool grow = j > 0 && mx > m_used + RESCALE_THRESHOLD;
       if (j == 0) {
         m_used = (mx == -INFINITY) ? 0.f : mx;
@@ -393,25 +503,24 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
         tc::tmem_wait_st();
         m_used = m_new;
       }
-      // pass 2: P = 2^(s*scale - m), bf16 pairs into the first 64 columns of S_i
+      // P = 2^(s*scale - m) as bf16 pairs into the first 64 columns of S_i
+      const float nm = -m_used;
+      float l8[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) l8[q] = 0.f;
 #pragma unroll
       for (int cb = 0; cb < BN / 32; ++cb) {
-        uint32_t v[32];
-        tc::tmem_ld32(tS + cb * 32, v);
-        tc::tmem_wait_ld();
         uint32_t pk[16];
 #pragma unroll
         for (int k = 0; k < 32; k += 2) {
-          const int kk = cb * 32 + k;
-          const bool v0 = full || ((uint32_t)(kk - a) >= span && kk < e);
-          const bool v1 = full || ((uint32_t)(kk + 1 - a) >= span && kk + 1 < e);
-          const float p0 = v0 ? tc::ex2(fmaf(__uint_as_float(v[k]), sl, -m_used)) : 0.f;
-          const float p1 = v1 ? tc::ex2(fmaf(__uint_as_float(v[k + 1]), sl, -m_used)) : 0.f;
-          l += p0 + p1;
+          const float p0 = tc::ex2(fmaf(__uint_as_float(v[cb * 32 + k]), sl, nm));
+          const float p1 = tc::ex2(fmaf(__uint_as_float(v[cb * 32 + k + 1]), sl, nm));
+          l8[(k >> 1) & 7] += p0 + p1;
           pk[k >> 1] = pack_bf16x2(p0, p1);
         }
         tc::tmem_st16(tS + cb * 16, pk);
       }
+      l += ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
       tc::tmem_wait_st();
       tc::tc_fence_before();
       tc::mbar_arrive(bar(B_PFULL + i));

@@ -38,32 +38,51 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                : "memory");
 }
 
+// A waiting thread sleeps in try_wait until the phase completes or this many
+// nanoseconds pass, instead of spinning.
+constexpr uint32_t kSuspendHintNs = 1000000;
+
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n"
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n"
       " selp.u32 %0, 1, 0, p;\n}\n"
       : "=r"(ok)
-      : "r"(bar), "r"(parity)
+      : "r"(bar), "r"(parity), "r"(kSuspendHintNs)
       : "memory");
   return ok != 0;
 }
 
-// Wait for the phase with the given parity to complete, for at most
-// limit_ns nanoseconds of global time.  Returns false (and raises *abort)
-// when the limit passes or another thread already raised *abort.
+// Wait for the phase with the given parity to complete.  The wait is bounded:
+// after limit_ns nanoseconds (counted in SM cycles at the 2.07 GHz maximum
+// clock, so a slower clock only lengthens it) it raises *abort and returns
+// false; it also returns false once another thread has raised *abort.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns,
                                           volatile int* abort) {
   if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer();
-  while (true) {
+  const long long limit = (long long)(limit_ns * 2.07);
+  const long long t0 = clock64();
+  for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (*abort) return false;
-    if (globaltimer() - t0 > limit_ns) {
-      *abort = 1;
-      return false;
+    if ((it & 63) == 0) {
+      if (*abort) return false;
+      if (clock64() - t0 > limit) {
+        *abort = 1;
+        return false;
+      }
     }
   }
+}
+
+// Re-split the register file between warpgroups (executed by all 128
+// threads of a warpgroup).
+template <int N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
 
 // ------------------------------------------------------------------ TMA
