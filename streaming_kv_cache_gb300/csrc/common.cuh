@@ -57,12 +57,12 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
-// Round two floats to fp16 (nearest even), clamped to +-65504, packed lo | hi << 16.
+// Round two floats to fp16 (nearest even), saturating to +-65504 instead of
+// overflowing, packed lo | hi << 16 (the convert takes the upper half first).
 __device__ __forceinline__ uint32_t pack_f16x2_sat(float lo, float hi) {
-  lo = fminf(fmaxf(lo, -65504.f), 65504.f);
-  hi = fminf(fmaxf(hi, -65504.f), 65504.f);
-  __half2 h = __floats2half2_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&h);
+  uint32_t r;
+  asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
 }
 
 __device__ __forceinline__ void set_status(int32_t* status, int bits) {

@@ -169,12 +169,14 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
   const Geom& g = p.g;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-  // work item: views in descending order (later views have more keys)
+  // work item: the V x chunks CTAs of one (cache, kv head) are adjacent, so
+  // they run together and share that plane's K/V tiles through L2; inside a
+  // plane the later (heavier) views come first
   int w = blockIdx.x;
   const int chunk = w % p.chunks;  w /= p.chunks;
+  const int vq = g.V - 1 - (w % g.V);  w /= g.V;
   const int h = w % g.Hkv;         w /= g.Hkv;
-  const int c = w % g.C;           w /= g.C;
-  const int vq = g.V - 1 - w;
+  const int c = w;
   const int t0 = chunk * 2 * p.TQ;                 // first token (within the view's newest frame)
   const int t_max = min(g.T, t0 + 2 * p.TQ) - 1;   // last valid token of the CTA
   const int32_t* head_c = p.head + (size_t)c * g.V;

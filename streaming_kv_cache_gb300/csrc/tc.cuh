@@ -74,6 +74,17 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_
   }
 }
 
+// A value the compiler must (re)compute where it stands: keeps loop-invariant
+// descriptors from being hoisted and held in registers across a loop.
+__device__ __forceinline__ uint64_t opaque(uint64_t x) {
+  asm volatile("mov.b64 %0, %0;" : "+l"(x));
+  return x;
+}
+__device__ __forceinline__ uint32_t opaque32(uint32_t x) {
+  asm volatile("mov.b32 %0, %0;" : "+r"(x));
+  return x;
+}
+
 // Re-split the register file between warpgroups (executed by all 128
 // threads of a warpgroup).
 template <int N>
