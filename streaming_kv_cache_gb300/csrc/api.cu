@@ -158,8 +158,8 @@ int stream_attn_prefill(const skv_cache* cache, int32_t n_q_head, const void* q_
 }
 
 size_t skv_verify_workspace_bytes(const skv_cache* cache, int32_t n_q_head, int32_t blk) {
-  (void)cache; (void)n_q_head; (void)blk;
-  return 0;
+  if (check_cache(cache) || n_q_head < 1 || n_q_head % cache->n_kv_head || blk < 1) return 0;
+  return skv::verify_ws_bytes(skv::geom_of(*cache), n_q_head, blk);
 }
 
 int stream_attn_verify(const skv_cache* cache, int32_t n_q_head, int32_t blk,
@@ -179,16 +179,17 @@ int stream_attn_verify(const skv_cache* cache, int32_t n_q_head, int32_t blk,
     return SKV_ERR_INVALID;
   const bool ids = target_ids && draft_ids;
   if (ids && (!accept_len || !next_token)) return SKV_ERR_INVALID;
-  if (ws_bytes < skv_verify_workspace_bytes(cache, n_q_head, blk)) return SKV_ERR_INVALID;
-  (void)ws;
+  const size_t ws_need = skv_verify_workspace_bytes(cache, n_q_head, blk);
+  if (ws_bytes < ws_need || (ws_need && (!ws || !aligned16(ws)))) return SKV_ERR_INVALID;
+  if (cache->n_view > 64) return SKV_ERR_UNSUPPORTED;   // the verify kernel keeps <= 64 ring heads on chip
   if ((rc = check_device())) return rc;
   const skv::Geom g = skv::geom_of(*cache);
   cudaStream_t st = (cudaStream_t)stream;
   cudaError_t e = skv::launch_write_rows(g, cache->k, cache->vt, k_blk, v_blk, 1, blk, 2, 0,
                                          cache->head, cache->sync, tail_len, cache->status, st);
   if (e != cudaSuccess) return cuda_fail(e);
-  e = skv::launch_attn_simple(g, n_q_head, 1, blk, q_blk, out, nullptr, tail_len, cache->k,
-                              cache->vt, cache->rope, cache->head, sm_scale, cache->status, st);
+  e = skv::launch_verify_tc(g, n_q_head, blk, tail_len, q_blk, out, cache->k, cache->vt, cache->rope,
+                            cache->head, ws, ws_bytes, sm_scale, cache->status, cache->wait_ns, st);
   if (e != cudaSuccess) return cuda_fail(e);
   if (ids) {
     e = skv::launch_accept(g.C, blk, target_ids, draft_ids, accept_len, next_token, st);

@@ -27,6 +27,12 @@ cudaError_t launch_prefill_tc(const Geom& g, int Hq, const void* q, void* out, f
                               const void* vt, const float* rope, const int32_t* head, float sm_scale,
                               int32_t* status, uint64_t wait_ns, cudaStream_t st);
 
+cudaError_t launch_verify_tc(const Geom& g, int Hq, int blk, const int32_t* tail_len, const void* q, void* out,
+                             const void* k, const void* vt, const float* rope, const int32_t* head,
+                             void* ws, size_t ws_bytes, float sm_scale, int32_t* status, uint64_t wait_ns,
+                             cudaStream_t st);
+size_t verify_ws_bytes(const Geom& g, int Hq, int blk);
+
 int check_insert_args(const skv_cache* cache, const void* k_new, const void* v_new);
 int record_cuda_error(cudaError_t e);
 

@@ -32,6 +32,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "rope.cuh"
 #include "tc.cuh"
 
 namespace skv {
@@ -89,67 +90,6 @@ struct PrefillParams {
   float scale_log2;
   uint64_t wait_ns;
 };
-
-// Rotate 8 bf16 pairs in fp32 and emit them as fp16: a holds elements x_e..x_{e+7},
-// b their partners x_{e+d/2}..; cs[k] = (cos, sin) of element e+k.  The rotated
-// Q and K feed an fp16 x fp16 tensor-core product (3 more significand bits
-// than bf16); values are clamped to the finite fp16 range.
-// t[w] = (cos, sin) of elements 2w and 2w+1 of the chunk.
-__device__ __forceinline__ void rotate_pairs4(uint4& a, uint4& b, const float4 (&t)[4]) {
-  uint32_t* pa = reinterpret_cast<uint32_t*>(&a);
-  uint32_t* pb = reinterpret_cast<uint32_t*>(&b);
-#pragma unroll
-  for (int w = 0; w < 4; ++w) {
-    const float x0 = bf16_lo(pa[w]), x1 = bf16_hi(pa[w]);
-    const float y0 = bf16_lo(pb[w]), y1 = bf16_hi(pb[w]);
-    pa[w] = pack_f16x2_sat(x0 * t[w].x - y0 * t[w].y, x1 * t[w].z - y1 * t[w].w);
-    pb[w] = pack_f16x2_sat(y0 * t[w].x + x0 * t[w].y, y1 * t[w].z + x1 * t[w].w);
-  }
-}
-
-__device__ __forceinline__ void rotate_pairs(uint4& a, uint4& b, const float2* __restrict__ cs) {
-  const float4* c4 = reinterpret_cast<const float4*>(cs);
-  float4 t[4];
-#pragma unroll
-  for (int w = 0; w < 4; ++w) t[w] = __ldg(c4 + w);
-  rotate_pairs4(a, b, t);
-}
-
-// Logical position of physical key row r and how many rows from r on (r
-// included) continue with consecutive positions: the rest of the prefix, of
-// the ring frame, or the tail.
-__device__ __forceinline__ void key_pos_run(const Geom& g, const int* __restrict__ heads, int r, int& pos,
-                                            int& run) {
-  const int u = r - g.P;
-  if (u < 0) {
-    pos = r;
-    run = g.P - r;
-    return;
-  }
-  if (u >= g.ring_rows()) {
-    pos = r;
-    run = 1 << 30;
-    return;
-  }
-  const int FT = g.F * g.T;
-  const int v = u / FT;
-  const int rem = u - v * FT;
-  const int sl = rem / g.T;
-  const int t = rem - sl * g.T;
-  int f = sl - heads[v];
-  if (f < 0) f += g.F;
-  pos = g.P + v * FT + f * g.T + t;
-  run = g.T - t;
-}
-
-__device__ __forceinline__ void advance_angles(float4 (&cs)[4], const float4 (&st)[4]) {
-#pragma unroll
-  for (int w = 0; w < 4; ++w) {
-    const float4 c = cs[w];
-    cs[w] = make_float4(c.x * st[w].x - c.y * st[w].y, c.y * st[w].x + c.x * st[w].y,
-                        c.z * st[w].z - c.w * st[w].w, c.w * st[w].z + c.z * st[w].w);
-  }
-}
 
 template <int D>
 __global__ void __launch_bounds__(NTHREADS, 1)
@@ -582,16 +522,18 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 }  // namespace
 
-// K: [C*Hkv][row_cap][d] -> boxes of 64 dims x 128 rows; V^T: [C*Hkv][d][row_cap]
-// -> boxes of 64 keys x d rows.  Both with the 128-byte swizzle.
-cudaError_t make_kv_tmaps(const Geom& g, const void* k, const void* vt, CUtensorMap* tk, CUtensorMap* tv) {
+// K: [C*Hkv][row_cap][d] -> boxes of 64 dims x k_box_rows rows; V^T:
+// [C*Hkv][d][row_cap] -> boxes of 64 keys x d rows.  Both with the 128-byte
+// swizzle.
+cudaError_t make_kv_tmaps(const Geom& g, const void* k, const void* vt, int k_box_rows, CUtensorMap* tk,
+                          CUtensorMap* tv) {
   auto fn = encode_fn();
   if (!fn) return cudaErrorNotSupported;
   const cuuint64_t planes = (cuuint64_t)g.C * g.Hkv;
   {
     cuuint64_t dims[3] = {(cuuint64_t)g.d, (cuuint64_t)g.row_cap, planes};
     cuuint64_t strides[2] = {(cuuint64_t)g.d * 2, (cuuint64_t)g.row_cap * g.d * 2};
-    cuuint32_t box[3] = {64, 128, 1};
+    cuuint32_t box[3] = {64, (cuuint32_t)k_box_rows, 1};
     cuuint32_t es[3] = {1, 1, 1};
     if (fn(tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(k), dims, strides, box, es,
            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -616,7 +558,7 @@ cudaError_t launch_prefill_tc(const Geom& g, int Hq, const void* q, void* out, f
                               int32_t* status, uint64_t wait_ns, cudaStream_t st) {
   if ((g.row_cap + BN - 1) / BN > MAX_TILES) return cudaErrorInvalidValue;
   CUtensorMap tk, tv;
-  cudaError_t e = make_kv_tmaps(g, k, vt, &tk, &tv);
+  cudaError_t e = make_kv_tmaps(g, k, vt, BN, &tk, &tv);
   if (e != cudaSuccess) return e;
   PrefillParams p;
   p.g = g;

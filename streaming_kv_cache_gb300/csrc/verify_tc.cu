@@ -1,0 +1,572 @@
+// stream_attn_verify on the tensor cores: split-K attention of a drafted
+// block over the streaming cache, HBM-bound, plus the combine of the splits.
+//
+// FlashDrive blog walkthrough, section 4.2: the target model checks a whole
+// drafted block in one forward pass; VFlash "03 · Generalist decoding": the
+// block holds one accepted anchor plus the proposals.  Block token j of
+// cache c sits at logical index P + V*F*T + tail_len[c] + j and sees every
+// key up to its own index (the block is causal within itself).
+//
+// One CTA = one (cache, kv head, key split).  Its 128-row query tile holds
+// the blk x G block rows of the kv head's query group (zero-padded), so the
+// MMA is M=128 with most rows idle: the kernel is bound by streaming K and
+// V^T from HBM, not by the tensor cores.  64-key tiles flow through 2-stage
+// TMA rings for K and V^T; RoPE is applied to each K tile in shared memory
+// (fp16 out), S double-buffers in TMEM so QK of tile j+1 overlaps the
+// softmax of tile j, and P (bf16) overwrites its S buffer for the PV MMA.
+// Each split leaves an unnormalised fp32 partial (O, running max m, sum l)
+// in the workspace; verify_combine merges them.  With a single split the
+// kernel writes the bf16 output itself.
+//
+//   warps 0-1  softmax + epilogue (TMEM lanes 0-63 = block rows)
+//   warp  2    K producer, TMEM allocator
+//   warp  3    V^T producer
+//   warp  4    MMA issuer
+//   warps 5-8  RoPE (query block once, then every K tile)
+#include <cudaTypedefs.h>
+#include <math.h>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "rope.cuh"
+#include "tc.cuh"
+
+namespace skv {
+
+namespace {
+
+constexpr int BM = 128;     // query-tile rows (block rows, zero-padded)
+constexpr int BN = 64;      // keys per tile
+constexpr int NTHREADS = 288;
+constexpr int WARP_KTMA = 2, WARP_VTMA = 3, WARP_MMA = 4, WARP_ROPE = 5;
+constexpr int SOFTMAX_THREADS = 64;
+constexpr int MAX_VIEWS = 64;
+constexpr float RESCALE_THRESHOLD = 8.0f;
+constexpr uint64_t DRAIN_NS = 500000000ull;
+
+template <int D>
+struct VLayout {
+  static constexpr int QT = BM * D * 2;
+  static constexpr int KT = BN * D * 2;   // 64 rows x D
+  static constexpr int VT = D * BN * 2;   // D rows x 64 keys (one 128-byte-swizzled box)
+  static constexpr int HALF_Q = BM * 128;
+  static constexpr int HALF_K = BN * 128;
+  static constexpr int Q_OFF = 0;
+  static constexpr int K_OFF = Q_OFF + QT;
+  static constexpr int V_OFF = K_OFF + 2 * KT;
+  static constexpr int BAR_OFF = V_OFF + 2 * VT;
+  static constexpr int NBAR = 18;
+  static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
+  static constexpr int HEAD_OFF = MISC_OFF + 32;
+  static constexpr int BYTES = HEAD_OFF + MAX_VIEWS * 4;
+  static constexpr int ALLOC = BYTES + 1024;
+};
+
+enum {
+  V_QFULL = 0, V_KFULL = 1, V_KROT = 3, V_KEMPTY = 5, V_VFULL = 7, V_VEMPTY = 9,
+  V_SFULL = 11, V_PFULL = 13, V_PVDONE = 15, V_ODONE = 16, V_DRAIN = 17, V_COUNT = 18
+};
+static_assert(VLayout<128>::NBAR == V_COUNT, "barrier slots");
+
+struct VerifyParams {
+  Geom g;
+  int Hq, G, blk, R;          // R = blk * G block rows per kv head
+  int splits, per;            // key splits per (cache, kv head), tiles per split
+  const int32_t* tail_len;
+  const uint16_t* q;          // [C][blk][Hq][D]
+  uint16_t* out;              // [C][blk][Hq][D]
+  float* ws_o;                // [C*Hkv*splits][R][D]
+  float* ws_ml;               // [C*Hkv*splits][R][2]
+  const float2* rope;
+  const int32_t* head;
+  int32_t* status;
+  float scale_log2;
+  uint64_t wait_ns;
+};
+
+template <int D>
+__global__ void __launch_bounds__(NTHREADS, 2)
+verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
+                 const VerifyParams p) {
+  using L = VLayout<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = tc::smem_u32(smem);
+  auto bar = [&](int i) { return sbase + L::BAR_OFF + 8u * i; };
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + L::MISC_OFF);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(smem + L::MISC_OFF + 4);
+  int* s_info = reinterpret_cast<int*>(smem + L::MISC_OFF + 8);   // nt, tile0, tail_len
+  int* s_head = reinterpret_cast<int*>(smem + L::HEAD_OFF);
+
+  const Geom& g = p.g;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int split = blockIdx.x % p.splits;
+  const int unit = blockIdx.x / p.splits;       // c * Hkv + h
+  const int h = unit % g.Hkv, c = unit / g.Hkv;
+  const int32_t* head_c = p.head + (size_t)c * g.V;
+  const uint64_t wait_ns = p.wait_ns;
+  const size_t pidx = (size_t)unit * p.splits + split;
+
+  if (tid == 0) {
+    for (int i = 0; i < L::NBAR; ++i) {
+      const bool many = i == V_QFULL || i == V_KROT || i == V_KROT + 1;
+      const bool soft = i == V_PFULL || i == V_PFULL + 1;
+      tc::mbar_init(bar(i), many ? 128 : soft ? SOFTMAX_THREADS : 1);
+    }
+    *s_abort = 0;
+    int ok = 1;
+    for (int v = 0; v < g.V; ++v) {
+      const int hv = head_c[v];
+      if (hv < 0 || hv >= g.F) ok = 0;
+      s_head[v] = hv;
+    }
+    if (!ok) set_status(p.status, SKV_DEV_BAD_HEAD);
+    const int tl = p.tail_len[c];
+    if (tl < 0 || tl + p.blk > g.tail_cap) ok = 0;   // reported by the tail write
+    int nt = 0, tile0 = 0;
+    if (ok) {
+      const int n_keys = g.n_visual() + tl + p.blk;
+      const int nt_unit = (n_keys + BN - 1) / BN;
+      tile0 = split * p.per;
+      nt = max(0, min(p.per, nt_unit - tile0));
+    }
+    s_info[0] = ok ? nt : -1;
+    s_info[1] = tile0;
+    s_info[2] = ok ? tl : 0;
+    tc::fence_barrier_init();
+  }
+  if (warp == WARP_KTMA) {
+    tc::tmem_alloc(tc::smem_u32(s_tmem), 256);
+    tc::tmem_relinquish();
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = *s_tmem;
+  const int nt = max(s_info[0], 0);
+  const bool unit_ok = s_info[0] >= 0;
+  const int tile0 = s_info[1];
+  const int tl = s_info[2];
+  const int q_base = g.n_visual() + tl;    // logical index of block token 0
+
+  if (warp == WARP_KTMA || warp == WARP_VTMA) {
+    // ------------------------------------------------------------ producers
+    const bool is_k = warp == WARP_KTMA;
+    if (lane == 0 && nt > 0) {
+      tc::prefetch_tmap(is_k ? &tmap_k : &tmap_v);
+      int issued = 0;
+      for (int j = 0; j < nt; ++j) {
+        const int s = j & 1, u = j >> 1, r0 = (tile0 + j) * BN;
+        const int zc = c * g.Hkv + h;
+        if (j >= 2 && !tc::mbar_wait(bar((is_k ? V_KEMPTY : V_VEMPTY) + s), (u - 1) & 1, wait_ns, s_abort))
+          break;
+        if (is_k) {
+          tc::mbar_arrive_expect_tx(bar(V_KFULL + s), L::KT);
+#pragma unroll
+          for (int hf = 0; hf < D / 64; ++hf)
+            tc::tma_load_3d(sbase + L::K_OFF + s * L::KT + hf * L::HALF_K, &tmap_k, bar(V_KFULL + s), hf * 64, r0, zc);
+        } else {
+          tc::mbar_arrive_expect_tx(bar(V_VFULL + s), L::VT);
+          tc::tma_load_3d(sbase + L::V_OFF + s * L::VT, &tmap_v, bar(V_VFULL + s), r0, 0, zc);
+        }
+        issued = j + 1;
+      }
+      if (*s_abort) {
+        set_status(p.status, SKV_DEV_TIMEOUT);
+        for (int j = max(0, issued - 2); j < issued; ++j) {
+          volatile int never = 0;
+          tc::mbar_wait(bar((is_k ? V_KFULL : V_VFULL) + (j & 1)), (j >> 1) & 1, DRAIN_NS, &never);
+        }
+      }
+    }
+  } else if (warp == WARP_MMA) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0 && nt > 0) {
+      constexpr uint32_t idesc_qk = tc::idesc_f16(BM, BN);
+      constexpr uint32_t idesc_pv = tc::idesc_bf16(BM, D);
+      const uint64_t dq0 = tc::sdesc_sw128(sbase + L::Q_OFF);
+      const uint64_t dk0 = tc::sdesc_sw128(sbase + L::K_OFF);
+      const uint64_t dv0 = tc::sdesc_sw128(sbase + L::V_OFF);
+      auto issue_qk = [&](int j) {
+        const uint64_t dk = tc::opaque(dk0 + ((uint32_t)((j & 1) * L::KT) >> 4));
+        const uint64_t dq = tc::opaque(dq0);
+        const uint32_t d_tmem = tmem + (j & 1) * BN;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t offq = ((kk >> 2) * L::HALF_Q + (kk & 3) * 32) >> 4;
+          const uint32_t offk = ((kk >> 2) * L::HALF_K + (kk & 3) * 32) >> 4;
+          tc::mma_ss(d_tmem, dq + offq, dk + offk, idesc_qk, kk > 0);
+        }
+      };
+      bool ok = true;
+      auto issue_pv = [&](int t) {
+        const int vs = t & 1, vu = t >> 1;
+        if (!(ok = tc::mbar_wait(bar(V_VFULL + vs), vu & 1, wait_ns, s_abort))) return;
+        if (!(ok = tc::mbar_wait(bar(V_PFULL + (t & 1)), (t >> 1) & 1, wait_ns, s_abort))) return;
+        tc::tc_fence_after();
+        const uint64_t dv = tc::opaque(dv0 + ((uint32_t)(vs * L::VT) >> 4));
+        const uint32_t a_tmem = tmem + (t & 1) * BN;
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk)
+          tc::mma_ts(tmem + 128, a_tmem + kk * 8, dv + (((kk & 3) * 32) >> 4), idesc_pv, (t > 0 || kk > 0) ? 1u : 0u);
+        tc::mma_commit(bar(V_PVDONE));
+        tc::mma_commit(bar(V_VEMPTY + vs));
+      };
+      ok = tc::mbar_wait(bar(V_QFULL), 0, wait_ns, s_abort);
+      for (int j = 0; ok && j < nt; ++j) {
+        const int ks = j & 1, ku = j >> 1;
+        if (!(ok = tc::mbar_wait(bar(V_KROT + ks), ku & 1, wait_ns, s_abort))) break;
+        tc::tc_fence_after();
+        issue_qk(j);
+        tc::mma_commit(bar(V_SFULL + (j & 1)));
+        tc::mma_commit(bar(V_KEMPTY + ks));
+        if (j >= 1) issue_pv(j - 1);
+      }
+      if (ok) issue_pv(nt - 1);
+      if (ok) tc::mma_commit(bar(V_ODONE));
+      if (!ok) set_status(p.status, SKV_DEV_TIMEOUT);
+      tc::mma_commit(bar(V_DRAIN));
+      volatile int never = 0;
+      tc::mbar_wait(bar(V_DRAIN), 0, DRAIN_NS, &never);
+    }
+  } else if (warp >= WARP_ROPE) {
+    // ----------------------------------------------------------------- RoPE
+    const int rt = tid - WARP_ROPE * 32;   // 0..127
+    constexpr int HALF = D / 2;
+    if (nt > 0) {
+      // query block: row n = (token n / G, head n % G) of this kv head's group
+      uint8_t* qt = smem + L::Q_OFF;
+      if (rt < p.R) {
+        const int jt = rt / p.G, gq = rt % p.G;
+        const uint16_t* qrow = p.q + (((size_t)c * p.blk + jt) * p.Hq + h * p.G + gq) * D;
+        const float2* cs = p.rope + (size_t)(q_base + jt) * HALF;
+#pragma unroll
+        for (int ch = 0; ch < HALF / 8; ++ch) {
+          uint4 a = *reinterpret_cast<const uint4*>(qrow + ch * 8);
+          uint4 b = *reinterpret_cast<const uint4*>(qrow + HALF + ch * 8);
+          rotate_pairs(a, b, cs + ch * 8);
+          const int ea = ch * 8, eb = HALF + ch * 8;
+          *reinterpret_cast<uint4*>(qt + (ea / 64) * L::HALF_Q + tc::sw128_off(rt, (ea % 64) / 8)) = a;
+          *reinterpret_cast<uint4*>(qt + (eb / 64) * L::HALF_Q + tc::sw128_off(rt, (eb % 64) / 8)) = b;
+        }
+      } else {
+        const uint4 z = make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int ch = 0; ch < D / 8; ++ch)
+          *reinterpret_cast<uint4*>(qt + (ch / 8) * L::HALF_Q + tc::sw128_off(rt, ch % 8)) = z;
+      }
+    }
+    tc::fence_proxy_async_smem();
+    tc::mbar_arrive(bar(V_QFULL));
+    // key tiles: chunk ch (8 frequencies) of NPT consecutive rows per thread
+    constexpr int NCH = HALF / 8;
+    constexpr int NPT = BN * NCH / 128;   // rows per thread
+    const int wr = rt >> 5, ln = rt & 31;
+    const int ch = ln % NCH;
+    const int row_base = wr * 16 + (ln / NCH) * NPT;
+    const int ea = ch * 8, eb = HALF + ch * 8;
+    const uint32_t off_a = (ea / 64) * L::HALF_K, off_b = (eb / 64) * L::HALF_K;
+    const int ca = (ea % 64) / 8, cb = (eb % 64) / 8;
+    const float4* rope4 = reinterpret_cast<const float4*>(p.rope);
+    float4 step[4];
+#pragma unroll
+    for (int w4 = 0; w4 < 4; ++w4) step[w4] = __ldg(rope4 + (HALF + ea) / 2 + w4);   // R(1)
+    const int row_lim = q_base + p.blk;   // rows at or beyond are not keys of this pass
+#pragma unroll 1
+    for (int j = 0; j < nt; ++j) {
+      const int s = j & 1, u = j >> 1;
+      if (!tc::mbar_wait(bar(V_KFULL + s), u & 1, wait_ns, s_abort)) {
+        set_status(p.status, SKV_DEV_TIMEOUT);
+        break;
+      }
+      const int r0 = (tile0 + j) * BN + row_base;
+      if (r0 < row_lim) {
+        uint8_t* kt = smem + L::K_OFF + s * L::KT;
+        int pos, run;
+        key_pos_run(g, s_head, r0, pos, run);
+        float4 cs[4];
+#pragma unroll
+        for (int w4 = 0; w4 < 4; ++w4) cs[w4] = __ldg(rope4 + ((size_t)pos * HALF + ea) / 2 + w4);
+#pragma unroll
+        for (int k = 0; k < NPT; ++k) {
+          const int r = r0 + k;
+          if (r >= row_lim) break;
+          if (k > 0) {
+            if (run > 1) {
+              --run;
+              ++pos;
+              advance_angles(cs, step);
+            } else {
+              key_pos_run(g, s_head, r, pos, run);
+#pragma unroll
+              for (int w4 = 0; w4 < 4; ++w4) cs[w4] = __ldg(rope4 + ((size_t)pos * HALF + ea) / 2 + w4);
+            }
+          }
+          const int row = row_base + k;
+          uint4* pa = reinterpret_cast<uint4*>(kt + off_a + tc::sw128_off(row, ca));
+          uint4* pb = reinterpret_cast<uint4*>(kt + off_b + tc::sw128_off(row, cb));
+          uint4 xa = *pa, xb = *pb;
+          rotate_pairs4(xa, xb, cs);
+          *pa = xa;
+          *pb = xb;
+        }
+      }
+      tc::fence_proxy_async_smem();
+      tc::mbar_arrive(bar(V_KROT + s));
+    }
+  } else {
+    // ------------------------------------------------- softmax + epilogue
+    const int row = warp * 32 + lane;            // TMEM lane = block row (warps 0, 1)
+    const uint32_t t_lane = (uint32_t)(warp * 32) << 16;
+    const uint32_t tO = tmem + t_lane + 128;
+    const bool valid = row < p.R;
+    const int jt = valid ? row / p.G : 0;
+    const int lim = q_base + jt;                 // largest key index this row may see
+    const float sl = p.scale_log2;
+    float m_used = -INFINITY, l = 0.f;
+    bool ok = true;
+#pragma unroll 1
+    for (int j = 0; j < nt; ++j) {
+      const int sb = j & 1;
+      ok = __all_sync(0xffffffffu, tc::mbar_wait(bar(V_SFULL + sb), (j >> 1) & 1, wait_ns, s_abort));
+      if (!ok) break;
+      tc::tc_fence_after();
+      const uint32_t tS = tmem + t_lane + sb * BN;
+      uint32_t v[BN];
+#pragma unroll
+      for (int cb = 0; cb < BN / 32; ++cb)
+        tc::tmem_ld32(tS + cb * 32, *reinterpret_cast<uint32_t(*)[32]>(v + cb * 32));
+      const int r0 = (tile0 + j) * BN;
+      tc::tmem_wait_ld();
+      if (!__all_sync(0xffffffffu, r0 + BN - 1 <= lim)) {
+#pragma unroll
+        for (int k = 0; k < BN; ++k)
+          if (r0 + k > lim) v[k] = __float_as_uint(-INFINITY);
+      }
+      float m8[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) m8[q] = __uint_as_float(v[q]);
+#pragma unroll
+      for (int k = 8; k < BN; ++k) m8[k & 7] = fmaxf(m8[k & 7], __uint_as_float(v[k]));
+      float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                       fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+      mx *= sl;
+      const bool grow = j > 0 && mx > m_used + RESCALE_THRESHOLD;
+      if (j == 0) {
+        m_used = (mx == -INFINITY) ? 0.f : mx;
+      } else if (__any_sync(0xffffffffu, grow)) {
+        // PV(j-1) must have landed in O before it is rescaled
+        ok = __all_sync(0xffffffffu, tc::mbar_wait(bar(V_PVDONE), (j - 1) & 1, wait_ns, s_abort));
+        if (!ok) break;
+        tc::tc_fence_after();
+        const float m_new = grow ? mx : m_used;
+        const float alpha = tc::ex2(m_used - m_new);
+        l *= alpha;
+#pragma unroll 1
+        for (int cb = 0; cb < D / 16; ++cb) {   // 16 columns at a time: the score row stays live
+          uint32_t o[16];
+          tc::tmem_ld16(tO + cb * 16, o);
+          tc::tmem_wait_ld();
+#pragma unroll
+          for (int k = 0; k < 16; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+          tc::tmem_st16(tO + cb * 16, o);
+        }
+        tc::tmem_wait_st();
+        m_used = m_new;
+      }
+      const float nm = -m_used;
+      float l8[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) l8[q] = 0.f;
+#pragma unroll
+      for (int cb = 0; cb < BN / 32; ++cb) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int k = 0; k < 32; k += 2) {
+          const float p0 = tc::ex2(fmaf(__uint_as_float(v[cb * 32 + k]), sl, nm));
+          const float p1 = tc::ex2(fmaf(__uint_as_float(v[cb * 32 + k + 1]), sl, nm));
+          l8[(k >> 1) & 7] += p0 + p1;
+          pk[k >> 1] = pack_bf16x2(p0, p1);
+        }
+        tc::tmem_st16(tS + cb * 16, pk);
+      }
+      l += ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
+      tc::tmem_wait_st();
+      tc::tc_fence_before();
+      tc::mbar_arrive(bar(V_PFULL + sb));
+    }
+    if (!ok) set_status(p.status, SKV_DEV_TIMEOUT);
+    bool done = ok && nt > 0;
+    if (done) done = __all_sync(0xffffffffu, tc::mbar_wait(bar(V_ODONE), 0, wait_ns, s_abort));
+    if (done) {
+      tc::tc_fence_after();
+      const int gq = valid ? row % p.G : 0;
+      if (p.splits == 1) {
+        const float inv_l = 1.f / l;
+        uint16_t* orow = p.out + (((size_t)c * p.blk + jt) * p.Hq + h * p.G + gq) * D;
+#pragma unroll 1
+        for (int cb = 0; cb < D / 32; ++cb) {
+          uint32_t o[32];
+          tc::tmem_ld32(tO + cb * 32, o);
+          tc::tmem_wait_ld();
+          if (valid) {
+            uint4 pk[4];
+            uint32_t* pw = reinterpret_cast<uint32_t*>(pk);
+#pragma unroll
+            for (int k = 0; k < 16; ++k)
+              pw[k] = pack_bf16x2(__uint_as_float(o[2 * k]) * inv_l, __uint_as_float(o[2 * k + 1]) * inv_l);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) reinterpret_cast<uint4*>(orow + cb * 32)[k] = pk[k];
+          }
+        }
+      } else {
+        float* orow = p.ws_o + (pidx * p.R + row) * D;
+#pragma unroll 1
+        for (int cb = 0; cb < D / 32; ++cb) {
+          uint32_t o[32];
+          tc::tmem_ld32(tO + cb * 32, o);
+          tc::tmem_wait_ld();
+          if (valid) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              reinterpret_cast<uint4*>(orow + cb * 32)[k] = make_uint4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
+          }
+        }
+        if (valid) {
+          p.ws_ml[(pidx * p.R + row) * 2] = m_used;
+          p.ws_ml[(pidx * p.R + row) * 2 + 1] = l;
+        }
+      }
+    } else if (nt == 0 && unit_ok && p.splits > 1 && valid) {
+      // a split past the unit's keys contributes nothing
+      p.ws_ml[(pidx * p.R + row) * 2] = -INFINITY;
+      p.ws_ml[(pidx * p.R + row) * 2 + 1] = 0.f;
+    } else if (nt > 0 && *s_abort) {
+      set_status(p.status, SKV_DEV_TIMEOUT);
+    }
+  }
+
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == WARP_KTMA) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem, 256);
+  }
+}
+
+// Merge the splits of every (cache, kv head, block row): one CTA per row,
+// one thread per head dimension.
+template <int D>
+__global__ void __launch_bounds__(D) verify_combine_kernel(const VerifyParams p) {
+  const int row = blockIdx.x % p.R;
+  const int unit = blockIdx.x / p.R;
+  const int h = unit % p.g.Hkv, c = unit / p.g.Hkv;
+  const int tl = p.tail_len[c];
+  if (tl < 0 || tl + p.blk > p.g.tail_cap) return;   // skipped cache (status set by the tail write)
+  const int d = threadIdx.x;
+  const size_t base = (size_t)unit * p.splits;
+  float M = -INFINITY;
+  for (int s = 0; s < p.splits; ++s) M = fmaxf(M, p.ws_ml[((base + s) * p.R + row) * 2]);
+  float num = 0.f, den = 0.f;
+  for (int s = 0; s < p.splits; ++s) {
+    const float m = p.ws_ml[((base + s) * p.R + row) * 2];
+    if (m == -INFINITY) continue;
+    const float w = exp2f(m - M);
+    den += w * p.ws_ml[((base + s) * p.R + row) * 2 + 1];
+    num += w * p.ws_o[((base + s) * p.R + row) * D + d];
+  }
+  const int jt = row / p.G, gq = row % p.G;
+  const __nv_bfloat16 b = __float2bfloat16_rn(num / den);
+  p.out[(((size_t)c * p.blk + jt) * p.Hq + h * p.G + gq) * D + d] = *reinterpret_cast<const uint16_t*>(&b);
+}
+
+int g_num_sms[64];
+
+int num_sms() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (!g_num_sms[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    g_num_sms[dev] = n;
+  }
+  return g_num_sms[dev];
+}
+
+}  // namespace
+
+// Split plan: enough CTAs for about eight per SM (two resident at a time),
+// never more splits than key tiles.
+void verify_plan(const Geom& g, int Hq, int blk, int* splits, int* per) {
+  const long long units = (long long)g.C * g.Hkv;
+  const int tiles_max = (g.n_visual() + g.tail_cap + BN - 1) / BN;
+  const long long target = 8LL * num_sms();
+  long long s = units > 0 ? (target + units - 1) / units : 1;
+  if (s < 1) s = 1;
+  if (s > tiles_max) s = tiles_max;
+  int pr = (int)((tiles_max + s - 1) / s);
+  *per = pr;
+  *splits = (tiles_max + pr - 1) / pr;
+  (void)Hq;
+  (void)blk;
+}
+
+size_t verify_ws_bytes(const Geom& g, int Hq, int blk) {
+  int splits, per;
+  verify_plan(g, Hq, blk, &splits, &per);
+  if (splits <= 1) return 0;
+  const size_t rows = (size_t)g.C * g.Hkv * splits * blk * (Hq / g.Hkv);
+  return rows * (g.d + 2) * sizeof(float) + 256;
+}
+
+cudaError_t make_kv_tmaps(const Geom& g, const void* k, const void* vt, int k_box_rows, CUtensorMap* tk,
+                          CUtensorMap* tv);
+
+cudaError_t launch_verify_tc(const Geom& g, int Hq, int blk, const int32_t* tail_len, const void* q, void* out,
+                             const void* k, const void* vt, const float* rope, const int32_t* head,
+                             void* ws, size_t ws_bytes, float sm_scale, int32_t* status, uint64_t wait_ns,
+                             cudaStream_t st) {
+  if (g.V > MAX_VIEWS) return cudaErrorNotSupported;
+  CUtensorMap tk, tv;
+  cudaError_t e = make_kv_tmaps(g, k, vt, BN, &tk, &tv);
+  if (e != cudaSuccess) return e;
+  VerifyParams p;
+  p.g = g;
+  p.Hq = Hq;
+  p.G = Hq / g.Hkv;
+  p.blk = blk;
+  p.R = blk * p.G;
+  verify_plan(g, Hq, blk, &p.splits, &p.per);
+  p.tail_len = tail_len;
+  p.q = static_cast<const uint16_t*>(q);
+  p.out = static_cast<uint16_t*>(out);
+  const size_t need = verify_ws_bytes(g, Hq, blk);
+  if (ws_bytes < need || (need && !ws)) return cudaErrorInvalidValue;
+  const size_t n_rows = (size_t)g.C * g.Hkv * p.splits * p.R;
+  p.ws_o = static_cast<float*>(ws);
+  p.ws_ml = need ? static_cast<float*>(ws) + n_rows * g.d : nullptr;
+  p.rope = reinterpret_cast<const float2*>(rope);
+  p.head = head;
+  p.status = status;
+  p.scale_log2 = sm_scale * 1.4426950408889634f;
+  p.wait_ns = wait_ns ? wait_ns : 2000000000ull;
+  const long long blocks = (long long)g.C * g.Hkv * p.splits;
+  if (blocks <= 0) return cudaSuccess;
+  if (blocks > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
+  if (g.d == 128) {
+    const int smem = VLayout<128>::ALLOC;
+    e = cudaFuncSetAttribute(verify_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    verify_tc_kernel<128><<<(unsigned)blocks, NTHREADS, smem, st>>>(tk, tv, p);
+    if (p.splits > 1) verify_combine_kernel<128><<<(unsigned)(g.C * g.Hkv * p.R), 128, 0, st>>>(p);
+  } else {
+    const int smem = VLayout<64>::ALLOC;
+    e = cudaFuncSetAttribute(verify_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    verify_tc_kernel<64><<<(unsigned)blocks, NTHREADS, smem, st>>>(tk, tv, p);
+    if (p.splits > 1) verify_combine_kernel<64><<<(unsigned)(g.C * g.Hkv * p.R), 64, 0, st>>>(p);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace skv
