@@ -275,33 +275,15 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
     tc::setmaxnreg_dec<REG_ROPE>();
     const int rt = tid - WARP_ROPE * 32;   // 0..127: row of the tile
     constexpr int HALF = D / 2;
-    // query tiles: rotate each row at its logical position and store it in
-    // the 128-byte-swizzled K-major layout the MMA reads
-#pragma unroll 1
-    for (int i = 0; i < 2; ++i) {
-      const int tok = t0 + i * p.TQ + rt / p.G;
-      const int gq = rt % p.G;
-      uint8_t* qt = smem + L::Q_OFF + i * L::QT;
-      if (tok < g.T) {
-        const int pos = g.P + vq * FT + (g.F - 1) * g.T + tok;
-        const uint16_t* qrow = p.q + (((size_t)c * (g.V * g.T) + vq * g.T + tok) * p.Hq + h * p.G + gq) * D;
-        const float2* cs = p.rope + (size_t)pos * HALF;
-#pragma unroll
-        for (int ch = 0; ch < HALF / 8; ++ch) {
-          uint4 a = *reinterpret_cast<const uint4*>(qrow + ch * 8);
-          uint4 b = *reinterpret_cast<const uint4*>(qrow + HALF + ch * 8);
-          rotate_pairs(a, b, cs + ch * 8);
-          const int ca = (ch * 8) / 64, cb = (HALF + ch * 8) / 64;
-          *reinterpret_cast<uint4*>(qt + ca * L::HALF_Q + tc::sw128_off(rt, (ch * 8 % 64) / 8)) = a;
-          *reinterpret_cast<uint4*>(qt + cb * L::HALF_Q + tc::sw128_off(rt, ((HALF + ch * 8) % 64) / 8)) = b;
-        }
-      } else {
-        const uint4 z = make_uint4(0, 0, 0, 0);
-#pragma unroll
-        for (int ch = 0; ch < D / 8; ++ch)
-          *reinterpret_cast<uint4*>(qt + (ch / 8) * L::HALF_Q + tc::sw128_off(rt, ch % 8)) = z;
-      }
-    }
+    // query tiles: row r of tile i = (token t0 + i*TQ + r/G, head r%G), rotated
+    // at its logical position (fp16, swizzled K-major)
+    load_rotate_q<D>(smem + L::Q_OFF, 2, L::QT, L::HALF_Q, p.rope, rt, [&](int rr, int& pos) -> const uint16_t* {
+      const int i = rr / 128, r = rr % 128;
+      const int tok = t0 + i * p.TQ + r / p.G;
+      pos = g.P + vq * FT + (g.F - 1) * g.T + tok;
+      if (tok >= g.T) return nullptr;
+      return p.q + (((size_t)c * (g.V * g.T) + vq * g.T + tok) * p.Hq + h * p.G + r % p.G) * D;
+    });
     tc::fence_proxy_async_smem();
     tc::mbar_arrive(bar(B_QFULL));
     // key tiles, rotated in place once TMA has landed them.  Thread (warp wr,
@@ -520,6 +502,19 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
+// Raise the kernel's dynamic shared-memory limit once per device.
+template <typename K>
+cudaError_t set_smem_once(K kernel, int bytes, int variant) {
+  static int done[64][2];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < 64 && done[dev][variant]) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev][variant] = 1;
+  return e;
+}
+
 }  // namespace
 
 // K: [C*Hkv][row_cap][d] -> boxes of 64 dims x k_box_rows rows; V^T:
@@ -579,13 +574,11 @@ cudaError_t launch_prefill_tc(const Geom& g, int Hq, const void* q, void* out, f
   if (blocks > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
   if (g.d == 128) {
     const int smem = Layout<128>::ALLOC;
-    e = cudaFuncSetAttribute(prefill_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
+    if ((e = set_smem_once(prefill_tc_kernel<128>, smem, 0)) != cudaSuccess) return e;
     prefill_tc_kernel<128><<<(unsigned)blocks, NTHREADS, smem, st>>>(tk, tv, p);
   } else {
     const int smem = Layout<64>::ALLOC;
-    e = cudaFuncSetAttribute(prefill_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
+    if ((e = set_smem_once(prefill_tc_kernel<64>, smem, 1)) != cudaSuccess) return e;
     prefill_tc_kernel<64><<<(unsigned)blocks, NTHREADS, smem, st>>>(tk, tv, p);
   }
   return cudaGetLastError();

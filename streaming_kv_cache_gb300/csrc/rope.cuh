@@ -74,3 +74,63 @@ __device__ __forceinline__ void advance_angles(float4 (&cs)[4], const float4 (&s
 }
 
 }  // namespace skv
+
+namespace skv {
+
+// Load n_tiles query tiles of 128 rows into shared memory, rotated at their
+// positions and stored as fp16 in the 128-byte-swizzled K-major layout
+// (tile t at dst + t*tile_bytes, 64-column halves half_bytes apart).  The
+// (row, 8-pair chunk) items are spread over the 128 calling threads and
+// fetched two at a time, so the global and table loads overlap.
+// row_src(r) returns the pre-RoPE bf16 row of tile row r (nullptr for a
+// padding row, which is zero-filled) and its position.
+template <int D, typename RowSrc>
+__device__ __forceinline__ void load_rotate_q(uint8_t* dst, int n_tiles, int tile_bytes, int half_bytes,
+                                              const float2* __restrict__ rope, int tid128, RowSrc row_src) {
+  constexpr int HALF = D / 2;
+  constexpr int NCH = HALF / 8;
+  constexpr int BATCH = 2;
+  const int n_items = n_tiles * 128 * NCH;
+  for (int i0 = tid128 * BATCH; i0 < n_items; i0 += 128 * BATCH) {
+    uint4 xa[BATCH], xb[BATCH];
+    float4 t[BATCH][4];
+    int rr[BATCH], cc[BATCH];
+    bool live[BATCH];
+#pragma unroll
+    for (int q = 0; q < BATCH; ++q) {
+      const int it = i0 + q;
+      rr[q] = it / NCH;
+      cc[q] = it % NCH;
+      live[q] = false;
+      if (it < n_items) {
+        int pos;
+        const uint16_t* src = row_src(rr[q], pos);
+        if (src) {
+          live[q] = true;
+          xa[q] = *reinterpret_cast<const uint4*>(src + cc[q] * 8);
+          xb[q] = *reinterpret_cast<const uint4*>(src + HALF + cc[q] * 8);
+          const float4* c4 = reinterpret_cast<const float4*>(rope + (size_t)pos * HALF + cc[q] * 8);
+#pragma unroll
+          for (int w = 0; w < 4; ++w) t[q][w] = __ldg(c4 + w);
+        }
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < BATCH; ++q) {
+      if (i0 + q >= n_items) continue;
+      if (live[q]) {
+        rotate_pairs4(xa[q], xb[q], t[q]);
+      } else {
+        xa[q] = make_uint4(0, 0, 0, 0);
+        xb[q] = xa[q];
+      }
+      const int tile = rr[q] / 128, row = rr[q] % 128;
+      const int ea = cc[q] * 8, eb = HALF + cc[q] * 8;
+      uint8_t* base = dst + tile * tile_bytes;
+      *reinterpret_cast<uint4*>(base + (ea / 64) * half_bytes + row * 128 + ((((ea % 64) / 8) ^ (row & 7)) << 4)) = xa[q];
+      *reinterpret_cast<uint4*>(base + (eb / 64) * half_bytes + row * 128 + ((((eb % 64) / 8) ^ (row & 7)) << 4)) = xb[q];
+    }
+  }
+}
+
+}  // namespace skv

@@ -15,8 +15,9 @@
 // (fp16 out), S double-buffers in TMEM so QK of tile j+1 overlaps the
 // softmax of tile j, and P (bf16) overwrites its S buffer for the PV MMA.
 // Each split leaves an unnormalised fp32 partial (O, running max m, sum l)
-// in the workspace; verify_combine merges them.  With a single split the
-// kernel writes the bf16 output itself.
+// in the workspace; the last split of a (cache, kv head) to finish merges
+// them (read back from L2) and writes the bf16 output.  With a single split
+// the kernel writes the output directly.
 //
 //   warps 0-1  softmax + epilogue (TMEM lanes 0-63 = block rows)
 //   warp  2    K producer, TMEM allocator
@@ -41,6 +42,7 @@ constexpr int NTHREADS = 288;
 constexpr int WARP_KTMA = 2, WARP_VTMA = 3, WARP_MMA = 4, WARP_ROPE = 5;
 constexpr int SOFTMAX_THREADS = 64;
 constexpr int MAX_VIEWS = 64;
+constexpr int MAX_SPLITS = 64;
 constexpr float RESCALE_THRESHOLD = 8.0f;
 constexpr uint64_t DRAIN_NS = 500000000ull;
 
@@ -67,6 +69,8 @@ enum {
   V_SFULL = 11, V_PFULL = 13, V_PVDONE = 15, V_ODONE = 16, V_DRAIN = 17, V_COUNT = 18
 };
 static_assert(VLayout<128>::NBAR == V_COUNT, "barrier slots");
+// the merge keeps 128 block rows x MAX_SPLITS weights in the K and V stages
+static_assert(2 * VLayout<64>::KT + 2 * VLayout<64>::VT >= 128 * MAX_SPLITS * 4, "merge scratch");
 
 struct VerifyParams {
   Geom g;
@@ -77,12 +81,75 @@ struct VerifyParams {
   uint16_t* out;              // [C][blk][Hq][D]
   float* ws_o;                // [C*Hkv*splits][R][D]
   float* ws_ml;               // [C*Hkv*splits][R][2]
+  int* ws_count;              // [C*Hkv] arrival counters, zero between calls
   const float2* rope;
   const int32_t* head;
   int32_t* status;
   float scale_log2;
   uint64_t wait_ns;
 };
+
+// Arrival of a split whose partial is stored (called by the 64 softmax
+// threads): the last split of the (cache, kv head) to arrive is told to merge
+// and leaves the counter at zero for the next call.
+__device__ __forceinline__ void arrive_split(const VerifyParams& p, int unit, int tid, int* s_flag) {
+  asm volatile("bar.sync 1, %0;" ::"r"(SOFTMAX_THREADS) : "memory");
+  if (tid == 0) {
+    __threadfence();
+    const int prev = atomicAdd(&p.ws_count[unit], 1);
+    const int last = prev == p.splits - 1;
+    if (last) {
+      p.ws_count[unit] = 0;
+      __threadfence();
+    }
+    s_flag[3] = last;
+  }
+}
+
+// O = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s over the splits of one
+// (cache, kv head), bf16 into the block rows; all threads of the CTA, with
+// wts (shared memory, R x splits floats) for the per-row split weights.
+template <int D>
+__device__ __noinline__ void merge_splits(const VerifyParams& p, int unit, int c, int h, int tid, float* wts) {
+  const size_t base = (size_t)unit * p.splits;
+  const int S = p.splits;
+  for (int row = tid; row < p.R; row += NTHREADS) {
+    float M = -INFINITY;
+#pragma unroll 8
+    for (int sp = 0; sp < S; ++sp) M = fmaxf(M, __ldcg(p.ws_ml + ((base + sp) * p.R + row) * 2));
+    float den = 0.f;
+#pragma unroll 8
+    for (int sp = 0; sp < S; ++sp) {
+      const float m = __ldcg(p.ws_ml + ((base + sp) * p.R + row) * 2);
+      const float w = m == -INFINITY ? 0.f : exp2f(m - M);
+      wts[row * S + sp] = w;
+      den += w * __ldcg(p.ws_ml + ((base + sp) * p.R + row) * 2 + 1);
+    }
+    const float inv = 1.f / den;
+    for (int sp = 0; sp < S; ++sp) wts[row * S + sp] *= inv;
+  }
+  __syncthreads();
+  for (int e = tid; e < p.R * (D / 4); e += NTHREADS) {
+    const int row = e / (D / 4), d4 = e % (D / 4);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+    for (int sp = 0; sp < S; ++sp) {
+      const float w = wts[row * S + sp];
+      const float4 o = __ldcg(reinterpret_cast<const float4*>(p.ws_o + ((base + sp) * p.R + row) * D) + d4);
+      if (w != 0.f) {
+        acc.x += w * o.x;
+        acc.y += w * o.y;
+        acc.z += w * o.z;
+        acc.w += w * o.w;
+      }
+    }
+    const int jt = row / p.G, gq = row % p.G;
+    uint2 pk;
+    pk.x = pack_bf16x2(acc.x, acc.y);
+    pk.y = pack_bf16x2(acc.z, acc.w);
+    *reinterpret_cast<uint2*>(p.out + (((size_t)c * p.blk + jt) * p.Hq + h * p.G + gq) * D + d4 * 4) = pk;
+  }
+}
 
 template <int D>
 __global__ void __launch_bounds__(NTHREADS, 2)
@@ -95,7 +162,8 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
   auto bar = [&](int i) { return sbase + L::BAR_OFF + 8u * i; };
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + L::MISC_OFF);
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + L::MISC_OFF + 4);
-  int* s_info = reinterpret_cast<int*>(smem + L::MISC_OFF + 8);   // nt, tile0, tail_len
+  // nt, tile0, tail_len, merge flag, epilogue flags of the two softmax warps
+  int* s_info = reinterpret_cast<int*>(smem + L::MISC_OFF + 8);
   int* s_head = reinterpret_cast<int*>(smem + L::HEAD_OFF);
 
   const Geom& g = p.g;
@@ -133,6 +201,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
     s_info[0] = ok ? nt : -1;
     s_info[1] = tile0;
     s_info[2] = ok ? tl : 0;
+    s_info[3] = 0;
     tc::fence_barrier_init();
   }
   if (warp == WARP_KTMA) {
@@ -235,26 +304,12 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
     constexpr int HALF = D / 2;
     if (nt > 0) {
       // query block: row n = (token n / G, head n % G) of this kv head's group
-      uint8_t* qt = smem + L::Q_OFF;
-      if (rt < p.R) {
-        const int jt = rt / p.G, gq = rt % p.G;
-        const uint16_t* qrow = p.q + (((size_t)c * p.blk + jt) * p.Hq + h * p.G + gq) * D;
-        const float2* cs = p.rope + (size_t)(q_base + jt) * HALF;
-#pragma unroll
-        for (int ch = 0; ch < HALF / 8; ++ch) {
-          uint4 a = *reinterpret_cast<const uint4*>(qrow + ch * 8);
-          uint4 b = *reinterpret_cast<const uint4*>(qrow + HALF + ch * 8);
-          rotate_pairs(a, b, cs + ch * 8);
-          const int ea = ch * 8, eb = HALF + ch * 8;
-          *reinterpret_cast<uint4*>(qt + (ea / 64) * L::HALF_Q + tc::sw128_off(rt, (ea % 64) / 8)) = a;
-          *reinterpret_cast<uint4*>(qt + (eb / 64) * L::HALF_Q + tc::sw128_off(rt, (eb % 64) / 8)) = b;
-        }
-      } else {
-        const uint4 z = make_uint4(0, 0, 0, 0);
-#pragma unroll
-        for (int ch = 0; ch < D / 8; ++ch)
-          *reinterpret_cast<uint4*>(qt + (ch / 8) * L::HALF_Q + tc::sw128_off(rt, ch % 8)) = z;
-      }
+      load_rotate_q<D>(smem + L::Q_OFF, 1, L::QT, L::HALF_Q, p.rope, rt, [&](int rr, int& pos) -> const uint16_t* {
+        const int jt = rr / p.G;
+        pos = q_base + (rr < p.R ? jt : 0);
+        if (rr >= p.R) return nullptr;
+        return p.q + (((size_t)c * p.blk + jt) * p.Hq + h * p.G + rr % p.G) * D;
+      });
     }
     tc::fence_proxy_async_smem();
     tc::mbar_arrive(bar(V_QFULL));
@@ -272,6 +327,19 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
 #pragma unroll
     for (int w4 = 0; w4 < 4; ++w4) step[w4] = __ldg(rope4 + (HALF + ea) / 2 + w4);   // R(1)
     const int row_lim = q_base + p.blk;   // rows at or beyond are not keys of this pass
+    // the first row's (cos, sin) of the next tile is fetched while the current one is rotated
+    int pf_pos = -1, pf_run = 0;
+    float4 pf[4];
+    auto fetch = [&](int jj) {
+      const int r = (tile0 + jj) * BN + row_base;
+      pf_pos = -1;
+      if (r < row_lim) {
+        key_pos_run(g, s_head, r, pf_pos, pf_run);
+#pragma unroll
+        for (int w4 = 0; w4 < 4; ++w4) pf[w4] = __ldg(rope4 + ((size_t)pf_pos * HALF + ea) / 2 + w4);
+      }
+    };
+    if (nt > 0) fetch(0);
 #pragma unroll 1
     for (int j = 0; j < nt; ++j) {
       const int s = j & 1, u = j >> 1;
@@ -279,14 +347,11 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         set_status(p.status, SKV_DEV_TIMEOUT);
         break;
       }
-      const int r0 = (tile0 + j) * BN + row_base;
-      if (r0 < row_lim) {
+      if (pf_pos >= 0) {
+        const int r0 = (tile0 + j) * BN + row_base;
         uint8_t* kt = smem + L::K_OFF + s * L::KT;
-        int pos, run;
-        key_pos_run(g, s_head, r0, pos, run);
-        float4 cs[4];
-#pragma unroll
-        for (int w4 = 0; w4 < 4; ++w4) cs[w4] = __ldg(rope4 + ((size_t)pos * HALF + ea) / 2 + w4);
+        int pos = pf_pos, run = pf_run;
+        float4 cs[4] = {pf[0], pf[1], pf[2], pf[3]};
 #pragma unroll
         for (int k = 0; k < NPT; ++k) {
           const int r = r0 + k;
@@ -311,6 +376,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
           *pb = xb;
         }
       }
+      if (j + 1 < nt) fetch(j + 1);
       tc::fence_proxy_async_smem();
       tc::mbar_arrive(bar(V_KROT + s));
     }
@@ -398,6 +464,10 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
     if (!ok) set_status(p.status, SKV_DEV_TIMEOUT);
     bool done = ok && nt > 0;
     if (done) done = __all_sync(0xffffffffu, tc::mbar_wait(bar(V_ODONE), 0, wait_ns, s_abort));
+    // both softmax warps take the same epilogue path (the merge below syncs them)
+    if (lane == 0) s_info[4 + warp] = done;
+    asm volatile("bar.sync 1, %0;" ::"r"(SOFTMAX_THREADS) : "memory");
+    done = s_info[4] && s_info[5];
     if (done) {
       tc::tc_fence_after();
       const int gq = valid ? row % p.G : 0;
@@ -436,11 +506,15 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
           p.ws_ml[(pidx * p.R + row) * 2] = m_used;
           p.ws_ml[(pidx * p.R + row) * 2 + 1] = l;
         }
+        arrive_split(p, unit, tid, s_info);
       }
-    } else if (nt == 0 && unit_ok && p.splits > 1 && valid) {
+    } else if (nt == 0 && unit_ok && p.splits > 1) {
       // a split past the unit's keys contributes nothing
-      p.ws_ml[(pidx * p.R + row) * 2] = -INFINITY;
-      p.ws_ml[(pidx * p.R + row) * 2 + 1] = 0.f;
+      if (valid) {
+        p.ws_ml[(pidx * p.R + row) * 2] = -INFINITY;
+        p.ws_ml[(pidx * p.R + row) * 2 + 1] = 0.f;
+      }
+      arrive_split(p, unit, tid, s_info);
     } else if (nt > 0 && *s_abort) {
       set_status(p.status, SKV_DEV_TIMEOUT);
     }
@@ -452,32 +526,11 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
     tc::tc_fence_after();
     tc::tmem_dealloc(tmem, 256);
   }
-}
-
-// Merge the splits of every (cache, kv head, block row): one CTA per row,
-// one thread per head dimension.
-template <int D>
-__global__ void __launch_bounds__(D) verify_combine_kernel(const VerifyParams p) {
-  const int row = blockIdx.x % p.R;
-  const int unit = blockIdx.x / p.R;
-  const int h = unit % p.g.Hkv, c = unit / p.g.Hkv;
-  const int tl = p.tail_len[c];
-  if (tl < 0 || tl + p.blk > p.g.tail_cap) return;   // skipped cache (status set by the tail write)
-  const int d = threadIdx.x;
-  const size_t base = (size_t)unit * p.splits;
-  float M = -INFINITY;
-  for (int s = 0; s < p.splits; ++s) M = fmaxf(M, p.ws_ml[((base + s) * p.R + row) * 2]);
-  float num = 0.f, den = 0.f;
-  for (int s = 0; s < p.splits; ++s) {
-    const float m = p.ws_ml[((base + s) * p.R + row) * 2];
-    if (m == -INFINITY) continue;
-    const float w = exp2f(m - M);
-    den += w * p.ws_ml[((base + s) * p.R + row) * 2 + 1];
-    num += w * p.ws_o[((base + s) * p.R + row) * D + d];
+  if (s_info[3]) {
+    __threadfence();
+    // the K/V stages are idle now: they hold the split weights
+    merge_splits<D>(p, unit, c, h, tid, reinterpret_cast<float*>(smem + L::K_OFF));
   }
-  const int jt = row / p.G, gq = row % p.G;
-  const __nv_bfloat16 b = __float2bfloat16_rn(num / den);
-  p.out[(((size_t)c * p.blk + jt) * p.Hq + h * p.G + gq) * D + d] = *reinterpret_cast<const uint16_t*>(&b);
 }
 
 int g_num_sms[64];
@@ -493,30 +546,60 @@ int num_sms() {
   return g_num_sms[dev];
 }
 
-}  // namespace
-
-// Split plan: enough CTAs for about eight per SM (two resident at a time),
-// never more splits than key tiles.
-void verify_plan(const Geom& g, int Hq, int blk, int* splits, int* per) {
-  const long long units = (long long)g.C * g.Hkv;
-  const int tiles_max = (g.n_visual() + g.tail_cap + BN - 1) / BN;
-  const long long target = 8LL * num_sms();
-  long long s = units > 0 ? (target + units - 1) / units : 1;
-  if (s < 1) s = 1;
-  if (s > tiles_max) s = tiles_max;
-  int pr = (int)((tiles_max + s - 1) / s);
-  *per = pr;
-  *splits = (tiles_max + pr - 1) / pr;
-  (void)Hq;
-  (void)blk;
+// Raise the kernel's dynamic shared-memory limit once per device.
+template <typename K>
+cudaError_t set_smem_once(K kernel, int bytes, int variant) {
+  static int done[64][2];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < 64 && done[dev][variant]) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev][variant] = 1;
+  return e;
 }
 
+}  // namespace
+
+// Split plan.  Two CTAs are resident per SM, so the grid runs in waves of
+// 2 * SMs CTAs.  A split of n key tiles costs about n + 3 tile times (set-up,
+// pipeline fill and the partial), and merging S splits about 2 + S/2; the
+// plan takes the split count with the smallest (number of waves) x (cost of
+// one split) + merge.  Fewer splits win ties.  At most MAX_SPLITS splits, so
+// the merge weights (block rows x splits floats) fit in the idle K/V stages.
+void verify_plan(const Geom& g, int Hq, int blk, int* splits, int* per) {
+  (void)Hq;
+  (void)blk;
+  const long long units = (long long)g.C * g.Hkv;
+  const int tiles_max = (g.n_visual() + g.tail_cap + BN - 1) / BN;
+  const long long wave = 2LL * num_sms();
+  long long best_s = 1, best_cost = -1;
+  for (long long s = 1; s <= tiles_max; ++s) {
+    const long long pr = (tiles_max + s - 1) / s;
+    const long long sp = (tiles_max + pr - 1) / pr;
+    if (sp != s) continue;
+    if (sp > MAX_SPLITS) continue;
+    const long long waves = (units * sp + wave - 1) / wave;
+    const long long cost = waves * (pr + 3) + (sp > 1 ? 2 + sp / 2 : 0);   // + the merge
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best_s = s;
+    }
+  }
+  const int pr = (int)((tiles_max + best_s - 1) / best_s);
+  *per = pr;
+  *splits = (tiles_max + pr - 1) / pr;
+}
+
+// Workspace: [units] int32 counters (256-byte aligned block), then the fp32
+// partial O rows and the (m, l) pairs.
 size_t verify_ws_bytes(const Geom& g, int Hq, int blk) {
   int splits, per;
   verify_plan(g, Hq, blk, &splits, &per);
   if (splits <= 1) return 0;
-  const size_t rows = (size_t)g.C * g.Hkv * splits * blk * (Hq / g.Hkv);
-  return rows * (g.d + 2) * sizeof(float) + 256;
+  const size_t units = (size_t)g.C * g.Hkv;
+  const size_t rows = units * splits * blk * (Hq / g.Hkv);
+  return (units * 4 + 255) / 256 * 256 + rows * (g.d + 2) * sizeof(float);
 }
 
 cudaError_t make_kv_tmaps(const Geom& g, const void* k, const void* vt, int k_box_rows, CUtensorMap* tk,
@@ -542,9 +625,11 @@ cudaError_t launch_verify_tc(const Geom& g, int Hq, int blk, const int32_t* tail
   p.out = static_cast<uint16_t*>(out);
   const size_t need = verify_ws_bytes(g, Hq, blk);
   if (ws_bytes < need || (need && !ws)) return cudaErrorInvalidValue;
-  const size_t n_rows = (size_t)g.C * g.Hkv * p.splits * p.R;
-  p.ws_o = static_cast<float*>(ws);
-  p.ws_ml = need ? static_cast<float*>(ws) + n_rows * g.d : nullptr;
+  const size_t units = (size_t)g.C * g.Hkv;
+  const size_t n_rows = units * p.splits * p.R;
+  p.ws_count = static_cast<int*>(ws);
+  p.ws_o = need ? reinterpret_cast<float*>(static_cast<char*>(ws) + (units * 4 + 255) / 256 * 256) : nullptr;
+  p.ws_ml = need ? p.ws_o + n_rows * g.d : nullptr;
   p.rope = reinterpret_cast<const float2*>(rope);
   p.head = head;
   p.status = status;
@@ -555,16 +640,12 @@ cudaError_t launch_verify_tc(const Geom& g, int Hq, int blk, const int32_t* tail
   if (blocks > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
   if (g.d == 128) {
     const int smem = VLayout<128>::ALLOC;
-    e = cudaFuncSetAttribute(verify_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
+    if ((e = set_smem_once(verify_tc_kernel<128>, smem, 0)) != cudaSuccess) return e;
     verify_tc_kernel<128><<<(unsigned)blocks, NTHREADS, smem, st>>>(tk, tv, p);
-    if (p.splits > 1) verify_combine_kernel<128><<<(unsigned)(g.C * g.Hkv * p.R), 128, 0, st>>>(p);
   } else {
     const int smem = VLayout<64>::ALLOC;
-    e = cudaFuncSetAttribute(verify_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
+    if ((e = set_smem_once(verify_tc_kernel<64>, smem, 1)) != cudaSuccess) return e;
     verify_tc_kernel<64><<<(unsigned)blocks, NTHREADS, smem, st>>>(tk, tv, p);
-    if (p.splits > 1) verify_combine_kernel<64><<<(unsigned)(g.C * g.Hkv * p.R), 64, 0, st>>>(p);
   }
   return cudaGetLastError();
 }

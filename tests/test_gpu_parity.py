@@ -249,3 +249,49 @@ def test_empty_cache_set_is_a_no_op():
     q = torch.empty((0, w.n_new, w.Hq, w.d), dtype=torch.bfloat16, device="cuda")
     out = skv.stream_attn_prefill(cache, q, w.sm_scale)
     assert out.numel() == 0
+
+
+def test_calls_are_graph_capturable():
+    """insert + prefill + verify captured into one CUDA graph and replayed
+    give the same bytes as the same calls made eagerly on a twin cache."""
+    w = W["tiny"].with_(C=2, blk=9)
+    twins = [Pair(w, "graph"), Pair(w, "graph")]
+    for t in twins:
+        t.fill()
+    k, v = synth.frame_kv(w, w.F, "graph")
+    q = synth.frame_q(w, w.F, "graph")
+    bq, bk, bv = synth.verify_block(w, "graph")
+    tgt, drf, _ = synth.planted_ids(w.C, w.blk, "graph")
+    dev = {n: to_dev(x) for n, x in dict(k=k, v=v, q=q, bq=bq, bk=bk, bv=bv).items()}
+    ids = (torch.from_numpy(tgt).cuda(), torch.from_numpy(drf).cuda())
+    outs = []
+    for n, t in enumerate(twins):
+        tail = torch.zeros((w.C,), dtype=torch.int32, device="cuda")
+        po = torch.empty_like(dev["q"])
+        vo = torch.empty_like(dev["bq"])
+        acc = torch.empty((w.C,), dtype=torch.int32, device="cuda")
+        nxt = torch.empty((w.C,), dtype=torch.int32, device="cuda")
+        ws = skv.verify_workspace(t.cache, w.Hq, w.blk)
+
+        def step():
+            skv.kv_stream_insert(t.cache, dev["k"], dev["v"])
+            skv.stream_attn_prefill(t.cache, dev["q"], w.sm_scale, out=po)
+            skv.stream_attn_verify(t.cache, tail, dev["bq"], dev["bk"], dev["bv"], w.sm_scale,
+                                   target_ids=ids[0], draft_ids=ids[1], ws=ws, out=vo,
+                                   accept_len=acc, next_token=nxt)
+        if n == 0:
+            step()
+        else:
+            g = torch.cuda.CUDAGraph()
+            side = torch.cuda.Stream()
+            side.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(side):
+                with torch.cuda.graph(g):
+                    step()
+            torch.cuda.current_stream().wait_stream(side)
+            g.replay()
+        torch.cuda.synchronize()
+        outs.append((po.clone(), vo.clone(), acc.clone(), t.cache.k.clone(), t.cache.head.clone()))
+    for a, b in zip(*outs):
+        assert torch.equal(a, b)
+    assert twins[1].cache.device_status() == 0
