@@ -494,10 +494,11 @@ def main():
                          "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
                          "frac": pre_tf / pk["bf16_tflops"], "peak_source": tag + " (burst)",
                          "frac_of_sustained": pre_tf / pk["bf16_tflops_sustained"],
-                         "traffic": traffic_for("attn_simple.cu")},
+                         "traffic": traffic_for("prefill_tc.cu")},
             "verify_roofline": {"bound": "hbm", "kernel": "stream_attn_verify", "achieved": ver_gbs,
                                 "peak": pk["hbm_gbs"], "unit": "GB/s",
-                                "frac": ver_gbs / pk["hbm_gbs"], "peak_source": tag},
+                                "frac": ver_gbs / pk["hbm_gbs"], "peak_source": tag,
+                                "traffic": traffic_for("verify_tc.cu")},
             "insert_roofline": {"bound": "hbm", "kernel": "kv_stream_insert", "achieved": ins_gbs,
                                 "peak": pk["hbm_gbs"], "unit": "GB/s",
                                 "frac": ins_gbs / pk["hbm_gbs"], "peak_source": tag},
