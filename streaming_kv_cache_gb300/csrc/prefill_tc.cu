@@ -1,4 +1,5 @@
-// stream_attn_prefill on the 5th-generation tensor cores (tcgen05 + TMEM).
+// stream_attn_prefill on the 5th-generation tensor cores (tcgen05 + TMEM),
+// CTA pairs with M = 256 pair MMAs.
 //
 // FlashDrive blog walkthrough, section 3.2 "View-Major Ordering" and 3.3
 // "RoPE Position Shift"; paper summary, "Streaming Inference": only the
@@ -6,25 +7,32 @@
 // earlier views, its own view's older frames and its own frame causally;
 // keys are cached pre-RoPE and rotated at their current logical position.
 //
-// One CTA = one (cache, kv head, view, chunk of 2*TQ new-frame tokens).  Its
-// 2 x 128 query rows pack TQ = 128/G tokens x the G query heads that share
-// the kv head (GQA), so every K/V tile feeds 256 rows.  Key tiles of 128
-// rows stream through a 2-stage TMA ring in physical (ring) order; softmax
-// is order-free, so only positions and the mask need logical indices.
+// A cluster of two CTAs handles one (cache, kv head, view, 4*TQ new-frame
+// tokens); each CTA owns 2 x 128 query rows that pack TQ = 128/G tokens x the
+// G query heads sharing the kv head (GQA).  Both CTAs walk the same list of
+// 128-key tiles in physical (ring) order -- softmax does not depend on key
+// order, so only positions and the mask need logical indices.  Each CTA
+// loads and rotates HALF of every tile: K rows [64*rank, 64*rank + 64) and
+// V^T dimension rows [D/2*rank, D/2*(rank+1)).  The even CTA issues the pair
+// MMAs (tcgen05.mma.cta_group::2, M = 256): S_i = Q_i K^T takes A = each
+// CTA's own query tile and B = the two K halves; O_i += P_i V takes A = each
+// CTA's P (TMEM) and B = the two V^T halves.  Commits reach the barriers of
+// both CTAs; the odd CTA's arrivals reach the even CTA's barriers across
+// the cluster.
 //
 //   warps 0-3   softmax + epilogue of query tile 0 (TMEM lanes = rows)
 //   warps 4-7   softmax + epilogue of query tile 1
-//   warp  8     TMA producer (K tile, V^T tile) and TMEM allocator
-//   warp  9     MMA issuer: S_i = Q_i K^T (smem x smem, fp16 rotated
-//               operands), O_i += P_i V (bf16 P from TMEM, bf16 V^T from smem)
-//   warps 10-11 idle (complete the third warpgroup)
-//   warps 12-15 RoPE: rotate Q once, then every K tile in shared memory
-//               between the TMA landing and the MMA
+//   warp  8     K producer (TMA) and TMEM allocator
+//   warp  9     MMA issuer (even CTA only)
+//   warp  10    forwards "V half landed" to the even CTA
+//   warp  11    V^T producer (TMA)
+//   warps 12-15 RoPE: rotate Q once, then this CTA's half of every K tile
+//               in shared memory between the TMA landing and the MMA
 // Registers are re-split per warpgroup with setmaxnreg: the softmax threads
-// hold a whole 128-score row (192 registers), the others shrink.
+// hold a whole 128-score row (176 registers), the others shrink.
 //
-// TMEM (512 columns): S0 [0,128) S1 [128,256) O0 [256,256+D) O1 [384,384+D);
-// P_i (bf16 pairs) overwrites the first 64 columns of S_i.
+// TMEM (512 columns per CTA): S0 [0,128) S1 [128,256) O0 [256,256+D)
+// O1 [384,384+D); P_i (bf16 pairs) overwrites the first 64 columns of S_i.
 // Online softmax in the exp2 domain with lazy rescaling: O and l are only
 // rescaled when a row's running max grows by more than 8 (factor 256).
 #include <cudaTypedefs.h>
@@ -39,11 +47,12 @@ namespace skv {
 
 namespace {
 
-constexpr int BM = 128;          // rows per query tile
-constexpr int BN = 128;          // keys per tile
-constexpr int NSTAGE = 2;
+constexpr int BM = 128;          // rows per query tile (per CTA)
+constexpr int BN = 128;          // keys per tile (pair)
+constexpr int HN = BN / 2;       // keys per tile loaded by one CTA
+constexpr int NST = 4;           // K and V stages
 constexpr int NTHREADS = 512;
-constexpr int WARP_TMA = 8, WARP_MMA = 9, WARP_ROPE = 12;
+constexpr int WARP_KTMA = 8, WARP_MMA = 9, WARP_VFWD = 10, WARP_VTMA = 11, WARP_ROPE = 12;
 // register split (launch: 512 threads x 128): 2 x 128 x 176 + 128 x 56 + 128 x 104 = 65536
 constexpr int REG_SOFTMAX = 176, REG_CTRL = 56, REG_ROPE = 104;
 static_assert(256 * REG_SOFTMAX + 128 * REG_CTRL + 128 * REG_ROPE == 65536, "register split");
@@ -54,16 +63,17 @@ constexpr uint64_t DRAIN_NS = 500000000ull;  // bounded wait for own in-flight c
 
 template <int D>
 struct Layout {
-  static constexpr int QT = BM * D * 2;   // bytes of one query tile
-  static constexpr int KT = BN * D * 2;   // bytes of one K tile
-  static constexpr int VT = D * BN * 2;   // bytes of one V^T tile
-  static constexpr int HALF_Q = BM * 128; // bytes of one 64-column half of a Q/K tile
-  static constexpr int HALF_V = D * 128;  // bytes of one 64-key half of a V^T tile
+  static constexpr int QT = BM * D * 2;     // bytes of one query tile
+  static constexpr int HALF_Q = BM * 128;   // one 64-column half of a query tile
+  static constexpr int KST = HN * D * 2;    // this CTA's K rows of a tile: 64 x D
+  static constexpr int HALF_K = HN * 128;   // one 64-column half of them
+  static constexpr int VST = (D / 2) * BN * 2;  // this CTA's V^T rows: D/2 x 128 keys
+  static constexpr int HALF_V = (D / 2) * 128;  // one 64-key half of them
   static constexpr int Q_OFF = 0;
   static constexpr int K_OFF = Q_OFF + 2 * QT;
-  static constexpr int V_OFF = K_OFF + NSTAGE * KT;
-  static constexpr int BAR_OFF = V_OFF + NSTAGE * VT;
-  static constexpr int NBAR = 18;
+  static constexpr int V_OFF = K_OFF + NST * KST;
+  static constexpr int BAR_OFF = V_OFF + NST * VST;
+  static constexpr int NBAR = 32;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
   static constexpr int HEAD_OFF = MISC_OFF + 64;     // ring heads of this cache (<= MAX_VIEWS)
   static constexpr int TILE_OFF = HEAD_OFF + MAX_VIEWS * 4;
@@ -71,16 +81,27 @@ struct Layout {
   static constexpr int ALLOC = BYTES + 1024;   // slack for 1024-byte alignment
 };
 
-// barrier slots
+// barrier slots.  "even" = lives in the even CTA only and counts the
+// arrivals of both CTAs; "pair" = completed by a pair-MMA commit in both.
 enum {
-  B_QFULL = 0, B_KFULL = 1, B_KROT = 3, B_KEMPTY = 5, B_VFULL = 7, B_VEMPTY = 9,
-  B_SFULL = 11, B_PFULL = 13, B_ODONE = 15, B_DRAIN = 17, B_COUNT = 18
+  B_QFULL = 0,                 // even: 2 x 4 RoPE warps (query tiles rotated)
+  B_KFULL = 1,                 // local: this CTA's K half landed (TMA)
+  B_KROT = B_KFULL + NST,      // even: 2 x 4 RoPE warps (K halves rotated)
+  B_KEMPTY = B_KROT + NST,     // pair: K stage free
+  B_VFULL = B_KEMPTY + NST,    // local: this CTA's V^T half landed (TMA)
+  B_VREADY = B_VFULL + NST,    // even: 2 forwarders (both V^T halves landed)
+  B_VEMPTY = B_VREADY + NST,   // pair: V stage free
+  B_SFULL = B_VEMPTY + NST,    // pair: S_i ready
+  B_PFULL = B_SFULL + 2,       // even: 2 x 4 softmax warps (P_i ready)
+  B_ODONE = B_PFULL + 2,       // pair: PV_i issued so far complete
+  B_DRAIN = B_ODONE + 2,       // pair: every MMA complete
+  B_COUNT = B_DRAIN + 1
 };
-static_assert(Layout<128>::NBAR == B_COUNT && Layout<64>::NBAR == B_COUNT, "barrier slots");
+static_assert(Layout<128>::NBAR >= B_COUNT && Layout<64>::NBAR >= B_COUNT, "barrier slots");
 
 struct PrefillParams {
   Geom g;
-  int Hq, G, TQ, chunks;   // chunks of 2*TQ tokens per view
+  int Hq, G, TQ, pairs;   // pairs of CTAs per view (each CTA: 2*TQ tokens)
   const uint16_t* q;
   uint16_t* out;
   float* lse;
@@ -92,7 +113,7 @@ struct PrefillParams {
 };
 
 template <int D>
-__global__ void __launch_bounds__(NTHREADS, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                   const PrefillParams p) {
   using L = Layout<D>;
@@ -108,17 +129,20 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
 
   const Geom& g = p.g;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t rank = tc::cluster_ctarank();       // 0 = even CTA (issues the MMAs)
+  // barriers in the even CTA, addressed across the cluster
+  auto bar_even = [&](int i) { return tc::map_to_cta(bar(i), 0); };
 
-  // work item: the V x chunks CTAs of one (cache, kv head) are adjacent, so
-  // they run together and share that plane's K/V tiles through L2; inside a
-  // plane the later (heavier) views come first
-  int w = blockIdx.x;
-  const int chunk = w % p.chunks;  w /= p.chunks;
+  // work item: the pairs of one (cache, kv head) are adjacent, so they run
+  // together and share that plane's K/V tiles through L2; inside a plane
+  // the later (heavier) views come first
+  int w = blockIdx.x >> 1;
+  const int pc = w % p.pairs;      w /= p.pairs;
   const int vq = g.V - 1 - (w % g.V);  w /= g.V;
   const int h = w % g.Hkv;         w /= g.Hkv;
   const int c = w;
-  const int t0 = chunk * 2 * p.TQ;                 // first token (within the view's newest frame)
-  const int t_max = min(g.T, t0 + 2 * p.TQ) - 1;   // last valid token of the CTA
+  const int t0 = (pc * 2 + (int)rank) * 2 * p.TQ;      // first token of this CTA
+  const int t_max = min(g.T, (pc + 1) * 4 * p.TQ) - 1;  // last token of the pair (shared tile list)
   const int32_t* head_c = p.head + (size_t)c * g.V;
   const int FT = g.F * g.T;
   const int row_end = g.P + (vq + 1) * FT;         // keys beyond are later views / tail
@@ -126,13 +150,16 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
   const uint64_t wait_ns = p.wait_ns;
 
   if (tid == 0) {
-    for (int i = 0; i < L::NBAR; ++i) {
-      const bool many = i == B_QFULL || i == B_KROT || i == B_KROT + 1 || i == B_PFULL || i == B_PFULL + 1;
-      tc::mbar_init(bar(i), many ? 128 : 1);   // 128 = one arrival per thread of a warpgroup
+    for (int i = 0; i < B_COUNT; ++i) {
+      // warpgroup-wide events arrive once per warp (after __syncwarp): 2 CTAs x 4 warps
+      int count = 1;
+      if (i == B_QFULL || (i >= B_KROT && i < B_KROT + NST) || i == B_PFULL || i == B_PFULL + 1) count = 8;
+      if (i >= B_VREADY && i < B_VREADY + NST) count = 2;
+      tc::mbar_init(bar(i), count);
     }
     *s_abort = 0;
     // tile list over physical key rows [0, row_end), skipping tiles made only
-    // of newest-frame rows that no query of this CTA may see
+    // of newest-frame rows that no query of the pair may see
     int ok = 1;
     for (int v = 0; v <= vq; ++v) {
       const int hv = head_c[v];
@@ -149,164 +176,190 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
         if (r0 >= inv_lo && r1 <= inv_hi) continue;
         s_tiles[n++] = r0;
       }
-    } else {
+    } else if (rank == 0) {
       set_status(p.status, SKV_DEV_BAD_HEAD);
     }
     *s_ntiles = n;
     tc::fence_barrier_init();
   }
-  if (warp == WARP_TMA) {
-    tc::tmem_alloc(tc::smem_u32(s_tmem), 512);
-    tc::tmem_relinquish();
+  if (warp == WARP_KTMA) {
+    tc::tmem_alloc_pair(tc::smem_u32(s_tmem), 512);
+    tc::tmem_relinquish_pair();
   }
   tc::tc_fence_before();
   __syncthreads();
+  tc::cluster_sync();          // barriers of both CTAs initialised before any cross-CTA arrival
   tc::tc_fence_after();
   const uint32_t tmem = *s_tmem;
   const int nt = *s_ntiles;
 
   if (warp >= 8 && warp < WARP_ROPE) {
     tc::setmaxnreg_dec<REG_CTRL>();
-  if (warp == WARP_TMA) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0 && nt > 0) {
-      tc::prefetch_tmap(&tmap_k);
-      tc::prefetch_tmap(&tmap_v);
-      int issued = 0;
-      for (int j = 0; j < nt; ++j) {
-        const int s = j & 1, u = j >> 1, r0 = s_tiles[j];
-        if (j >= NSTAGE && !tc::mbar_wait(bar(B_KEMPTY + s), (u - 1) & 1, wait_ns, s_abort)) break;
-        tc::mbar_arrive_expect_tx(bar(B_KFULL + s), L::KT);
+    if (warp == WARP_KTMA || warp == WARP_VTMA) {
+      // -------------------------------------- producers of this CTA's halves
+      const bool is_k = warp == WARP_KTMA;
+      if (lane == 0 && nt > 0) {
+        tc::prefetch_tmap(is_k ? &tmap_k : &tmap_v);
+        int issued = 0;
+        for (int j = 0; j < nt; ++j) {
+          const int s = j % NST, u = j / NST, r0 = s_tiles[j];
+          if (j >= NST &&
+              !tc::mbar_wait_cluster(bar((is_k ? B_KEMPTY : B_VEMPTY) + s), (u - 1) & 1, wait_ns, s_abort))
+            break;
+          if (is_k) {
+            tc::mbar_arrive_expect_tx(bar(B_KFULL + s), L::KST);
 #pragma unroll
-        for (int hf = 0; hf < D / 64; ++hf)
-          tc::tma_load_3d(sbase + L::K_OFF + s * L::KT + hf * L::HALF_Q, &tmap_k, bar(B_KFULL + s), hf * 64, r0, zc);
-        if (j >= NSTAGE && !tc::mbar_wait(bar(B_VEMPTY + s), (u - 1) & 1, wait_ns, s_abort)) {
-          issued = j + 1;   // the K load of tile j is in flight
-          break;
-        }
-        tc::mbar_arrive_expect_tx(bar(B_VFULL + s), L::VT);
+            for (int hf = 0; hf < D / 64; ++hf)
+              tc::tma_load_3d(sbase + L::K_OFF + s * L::KST + hf * L::HALF_K, &tmap_k, bar(B_KFULL + s), hf * 64,
+                              r0 + HN * (int)rank, zc);
+          } else {
+            tc::mbar_arrive_expect_tx(bar(B_VFULL + s), L::VST);
 #pragma unroll
-        for (int hf = 0; hf < 2; ++hf)
-          tc::tma_load_3d(sbase + L::V_OFF + s * L::VT + hf * L::HALF_V, &tmap_v, bar(B_VFULL + s), r0 + hf * 64, 0, zc);
-        issued = j + 1;
-      }
-      if (*s_abort) {
-        set_status(p.status, SKV_DEV_TIMEOUT);
-        // let the copies this thread started land before the CTA exits
-        for (int j = max(0, issued - NSTAGE); j < issued; ++j) {
-          const int s = j & 1, u = j >> 1;
-          volatile int never = 0;
-          tc::mbar_wait(bar(B_KFULL + s), u & 1, DRAIN_NS, &never);
-          tc::mbar_wait(bar(B_VFULL + s), u & 1, DRAIN_NS, &never);
+            for (int kh = 0; kh < 2; ++kh)
+              tc::tma_load_3d(sbase + L::V_OFF + s * L::VST + kh * L::HALF_V, &tmap_v, bar(B_VFULL + s),
+                              r0 + kh * 64, (D / 2) * (int)rank, zc);
+          }
+          issued = j + 1;
+        }
+        if (*s_abort) {
+          set_status(p.status, SKV_DEV_TIMEOUT);
+          // let the copies this thread started land before the CTA exits
+          for (int j = max(0, issued - NST); j < issued; ++j) {
+            volatile int never = 0;
+            tc::mbar_wait(bar((is_k ? B_KFULL : B_VFULL) + j % NST), (j / NST) & 1, DRAIN_NS, &never);
+          }
         }
       }
-    }
-  } else if (warp == WARP_MMA) {
-    // ---------------------------------------------------------- MMA issuer
-    if (lane == 0 && nt > 0) {
-      constexpr uint32_t idesc_qk = tc::idesc_f16(BM, BN);
-      constexpr uint32_t idesc_pv = tc::idesc_bf16(BM, D);
-      // descriptors advance by adding (byte offset >> 4) to the start-address field
-      const uint64_t dq0 = tc::sdesc_sw128(sbase + L::Q_OFF);
-      const uint64_t dk0 = tc::sdesc_sw128(sbase + L::K_OFF);
-      const uint64_t dv0 = tc::sdesc_sw128(sbase + L::V_OFF);
-      auto issue_qk = [&](int i, int s) {
-        const uint64_t dq = dq0 + ((uint32_t)(i * L::QT) >> 4);
-        const uint64_t dk = dk0 + ((uint32_t)(s * L::KT) >> 4);
-#pragma unroll 1
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = ((kk >> 2) * L::HALF_Q + (kk & 3) * 32) >> 4;
-          tc::mma_ss(tmem + i * 128, dq + off, dk + off, idesc_qk, kk > 0);
+    } else if (warp == WARP_VFWD) {
+      // ------------------- tell the even CTA when this CTA's V^T half landed
+      if (lane == 0 && nt > 0) {
+        for (int j = 0; j < nt; ++j) {
+          const int s = j % NST, u = j / NST;
+          if (!tc::mbar_wait(bar(B_VFULL + s), u & 1, wait_ns, s_abort)) {
+            set_status(p.status, SKV_DEV_TIMEOUT);
+            break;
+          }
+          tc::mbar_arrive_cluster(bar_even(B_VREADY + s));
         }
-      };
-      auto issue_pv = [&](int i, int s, bool acc) {
-        const uint64_t dv = dv0 + ((uint32_t)(s * L::VT) >> 4);
-#pragma unroll 1
-        for (int kk = 0; kk < BN / 16; ++kk) {
-          const uint32_t off = ((kk >> 2) * L::HALF_V + (kk & 3) * 32) >> 4;
-          tc::mma_ts(tmem + 256 + i * 128, tmem + i * 128 + kk * 8, dv + off, idesc_pv,
-                     (acc || kk > 0) ? 1u : 0u);
-        }
-      };
-      bool ok = tc::mbar_wait(bar(B_QFULL), 0, wait_ns, s_abort);
-      if (ok) ok = tc::mbar_wait(bar(B_KROT), 0, wait_ns, s_abort);
-      if (ok) {
-        tc::tc_fence_after();
-        issue_qk(0, 0);
-        tc::mma_commit(bar(B_SFULL));
-        issue_qk(1, 0);
-        tc::mma_commit(bar(B_SFULL + 1));
-        tc::mma_commit(bar(B_KEMPTY));
       }
-      for (int j = 0; ok && j < nt; ++j) {
-        const int s = j & 1, u = j >> 1;
-        const int s2 = (j + 1) & 1, u2 = (j + 1) >> 1;
-        if (!(ok = tc::mbar_wait(bar(B_VFULL + s), u & 1, wait_ns, s_abort))) break;
-        if (!(ok = tc::mbar_wait(bar(B_PFULL), j & 1, wait_ns, s_abort))) break;
-        tc::tc_fence_after();
-        issue_pv(0, s, j > 0);
-        tc::mma_commit(bar(B_ODONE));
-        if (j + 1 < nt) {
-          if (!(ok = tc::mbar_wait(bar(B_KROT + s2), u2 & 1, wait_ns, s_abort))) break;
+    } else if (warp == WARP_MMA) {
+      // ------------------------------------------ MMA issuer (even CTA only)
+      if (lane == 0 && nt > 0 && rank == 0) {
+        constexpr uint32_t idesc_qk = tc::idesc_f16(2 * BM, BN);
+        constexpr uint32_t idesc_pv = tc::idesc_bf16(2 * BM, D);
+        // descriptors advance by adding (byte offset >> 4) to the start-address field;
+        // each CTA's operands sit at the same offsets in its own shared memory.
+        // The k-steps are unrolled (one thread must stay ahead of the tensor
+        // cores); each issue re-materialises its base descriptors (opaque
+        // move) so the compiler does not hoist every descriptor of the loop
+        // into registers.
+        const uint64_t dq0 = tc::sdesc_sw128(sbase + L::Q_OFF);
+        const uint64_t dk0 = tc::sdesc_sw128(sbase + L::K_OFF);
+        const uint64_t dv0 = tc::sdesc_sw128(sbase + L::V_OFF);
+        auto issue_qk = [&](int i, int s) {
+          const uint64_t dq = tc::opaque(dq0 + ((uint32_t)(i * L::QT) >> 4));
+          const uint64_t dk = tc::opaque(dk0 + ((uint32_t)(s * L::KST) >> 4));
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t oq = ((kk >> 2) * L::HALF_Q + (kk & 3) * 32) >> 4;
+            const uint32_t ok = ((kk >> 2) * L::HALF_K + (kk & 3) * 32) >> 4;
+            tc::mma_ss_pair(tmem + i * 128, dq + oq, dk + ok, idesc_qk, kk > 0);
+          }
+        };
+        auto issue_pv = [&](int i, int s, bool acc) {
+          const uint64_t dv = tc::opaque(dv0 + ((uint32_t)(s * L::VST) >> 4));
+#pragma unroll
+          for (int kk = 0; kk < BN / 16; ++kk) {
+            const uint32_t ov = ((kk >> 2) * L::HALF_V + (kk & 3) * 32) >> 4;
+            tc::mma_ts_pair(tmem + 256 + i * 128, tmem + i * 128 + kk * 8, dv + ov, idesc_pv,
+                            (acc || kk > 0) ? 1u : 0u);
+          }
+        };
+        bool ok = tc::mbar_wait_cluster(bar(B_QFULL), 0, wait_ns, s_abort);
+        if (ok) ok = tc::mbar_wait_cluster(bar(B_KROT), 0, wait_ns, s_abort);
+        if (ok) {
           tc::tc_fence_after();
-          issue_qk(0, s2);
-          tc::mma_commit(bar(B_SFULL));
+          issue_qk(0, 0);
+          tc::mma_commit_pair(bar(B_SFULL));
+          issue_qk(1, 0);
+          tc::mma_commit_pair(bar(B_SFULL + 1));
+          tc::mma_commit_pair(bar(B_KEMPTY));
         }
-        if (!(ok = tc::mbar_wait(bar(B_PFULL + 1), j & 1, wait_ns, s_abort))) break;
-        tc::tc_fence_after();
-        issue_pv(1, s, j > 0);
-        tc::mma_commit(bar(B_ODONE + 1));
-        tc::mma_commit(bar(B_VEMPTY + s));
-        if (j + 1 < nt) {
-          issue_qk(1, s2);
-          tc::mma_commit(bar(B_SFULL + 1));
-          tc::mma_commit(bar(B_KEMPTY + s2));
+        for (int j = 0; ok && j < nt; ++j) {
+          const int s = j % NST, u = j / NST;
+          const int s2 = (j + 1) % NST, u2 = (j + 1) / NST;
+          if (!(ok = tc::mbar_wait_cluster(bar(B_VREADY + s), u & 1, wait_ns, s_abort))) break;
+          if (!(ok = tc::mbar_wait_cluster(bar(B_PFULL), j & 1, wait_ns, s_abort))) break;
+          tc::tc_fence_after();
+          issue_pv(0, s, j > 0);
+          tc::mma_commit_pair(bar(B_ODONE));
+          if (j + 1 < nt) {
+            if (!(ok = tc::mbar_wait_cluster(bar(B_KROT + s2), u2 & 1, wait_ns, s_abort))) break;
+            tc::tc_fence_after();
+            issue_qk(0, s2);
+            tc::mma_commit_pair(bar(B_SFULL));
+          }
+          if (!(ok = tc::mbar_wait_cluster(bar(B_PFULL + 1), j & 1, wait_ns, s_abort))) break;
+          tc::tc_fence_after();
+          issue_pv(1, s, j > 0);
+          tc::mma_commit_pair(bar(B_ODONE + 1));
+          tc::mma_commit_pair(bar(B_VEMPTY + s));
+          if (j + 1 < nt) {
+            issue_qk(1, s2);
+            tc::mma_commit_pair(bar(B_SFULL + 1));
+            tc::mma_commit_pair(bar(B_KEMPTY + s2));
+          }
         }
+        if (!ok) set_status(p.status, SKV_DEV_TIMEOUT);
+        // every MMA issued completes (in both CTAs' TMEM) before TMEM is released
+        tc::mma_commit_pair(bar(B_DRAIN));
       }
-      if (!ok) set_status(p.status, SKV_DEV_TIMEOUT);
-      // every MMA this thread issued completes before TMEM is released
-      tc::mma_commit(bar(B_DRAIN));
-      volatile int never = 0;
-      tc::mbar_wait(bar(B_DRAIN), 0, DRAIN_NS, &never);
+      if (lane == 0 && nt > 0) {
+        volatile int never = 0;
+        tc::mbar_wait_cluster(bar(B_DRAIN), 0, DRAIN_NS, &never);
+      }
     }
-  }
   } else if (warp >= WARP_ROPE) {
     // ----------------------------------------------------------------- RoPE
     tc::setmaxnreg_dec<REG_ROPE>();
-    const int rt = tid - WARP_ROPE * 32;   // 0..127: row of the tile
+    const int rt = tid - WARP_ROPE * 32;   // 0..127
     constexpr int HALF = D / 2;
     // query tiles: row r of tile i = (token t0 + i*TQ + r/G, head r%G), rotated
     // at its logical position (fp16, swizzled K-major)
     load_rotate_q<D>(smem + L::Q_OFF, 2, L::QT, L::HALF_Q, p.rope, rt, [&](int rr, int& pos) -> const uint16_t* {
       const int i = rr / 128, r = rr % 128;
       const int tok = t0 + i * p.TQ + r / p.G;
-      pos = g.P + vq * FT + (g.F - 1) * g.T + tok;
+      pos = g.P + vq * FT + (g.F - 1) * g.T + min(tok, g.T - 1);
       if (tok >= g.T) return nullptr;
       return p.q + (((size_t)c * (g.V * g.T) + vq * g.T + tok) * p.Hq + h * p.G + r % p.G) * D;
     });
-    tc::fence_proxy_async_smem();
-    tc::mbar_arrive(bar(B_QFULL));
-    // key tiles, rotated in place once TMA has landed them.  Thread (warp wr,
-    // lane ln) takes chunk ch = ln % NCH (8 frequencies) of NCH consecutive
-    // rows; inside a frame consecutive rows have consecutive positions, so
-    // their (cos, sin) advance by one complex multiplication with R(1)
-    // instead of a table load.  The first row's table entries of the next
-    // tile are fetched while the current tile is rotated.
+    tc::fence_proxy_async();
+    __syncwarp();
+    tc::mbar_arrive_cluster_if(bar_even(B_QFULL), lane == 0);
+    // this CTA's 64 rows of every key tile, rotated in place once TMA has
+    // landed them.  Thread (warp wr, lane ln) takes chunk ch = ln % NCH (8
+    // frequencies) of NPT consecutive rows; inside a frame consecutive rows
+    // have consecutive positions, so their (cos, sin) advance by one complex
+    // multiplication with R(1) instead of a table load.  The first row's
+    // table entries of the next tile are fetched while the current tile is
+    // rotated.
     constexpr int NCH = HALF / 8;
+    constexpr int NPT = HN * NCH / 128;   // rows per thread
     const int wr = rt >> 5, ln = rt & 31;
     const int ch = ln % NCH;
-    const int row_base = wr * 32 + (ln / NCH) * NCH;
+    const int row_base = wr * (HN / 4) + (ln / NCH) * NPT;
     const int ea = ch * 8, eb = HALF + ch * 8;
-    const uint32_t off_a = (ea / 64) * L::HALF_Q, off_b = (eb / 64) * L::HALF_Q;
+    const uint32_t off_a = (ea / 64) * L::HALF_K, off_b = (eb / 64) * L::HALF_K;
     const int ca = (ea % 64) / 8, cb = (eb % 64) / 8;
     const float4* rope4 = reinterpret_cast<const float4*>(p.rope);
     float4 step[4];
 #pragma unroll
     for (int w4 = 0; w4 < 4; ++w4) step[w4] = __ldg(rope4 + (HALF + ea) / 2 + w4);   // R(1)
+    const int row0 = HN * (int)rank + row_base;       // this thread's first row inside a tile
     int pf_pos = -1, pf_run = 0;
     float4 pf[4];
     auto fetch = [&](int jj) {
-      const int r = s_tiles[jj] + row_base;
+      const int r = s_tiles[jj] + row0;
       pf_pos = -1;
       if (r < row_end) {
         key_pos_run(g, s_head, r, pf_pos, pf_run);
@@ -317,18 +370,18 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
     if (nt > 0) fetch(0);
 #pragma unroll 1
     for (int j = 0; j < nt; ++j) {
-      const int s = j & 1, u = j >> 1;
+      const int s = j % NST, u = j / NST;
       if (!tc::mbar_wait(bar(B_KFULL + s), u & 1, wait_ns, s_abort)) {
         set_status(p.status, SKV_DEV_TIMEOUT);
         break;
       }
       if (pf_pos >= 0) {
-        uint8_t* kt = smem + L::K_OFF + s * L::KT;
-        const int r0 = s_tiles[j] + row_base;
+        uint8_t* kt = smem + L::K_OFF + s * L::KST;
+        const int r0 = s_tiles[j] + row0;
         int pos = pf_pos, run = pf_run;
         float4 cs[4] = {pf[0], pf[1], pf[2], pf[3]};
 #pragma unroll
-        for (int k = 0; k < NCH; ++k) {
+        for (int k = 0; k < NPT; ++k) {
           const int r = r0 + k;
           if (r >= row_end) break;
           if (k > 0) {
@@ -352,8 +405,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
         }
       }
       if (j + 1 < nt) fetch(j + 1);
-      tc::fence_proxy_async_smem();
-      tc::mbar_arrive(bar(B_KROT + s));
+      tc::fence_proxy_async();
+      __syncwarp();
+      tc::mbar_arrive_cluster_if(bar_even(B_KROT + s), lane == 0);
     }
   } else {
     // ------------------------------------------------- softmax + epilogue
@@ -379,7 +433,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
 #pragma unroll 1
     for (int j = 0; j < nt; ++j) {
       // tcgen05.ld/st below are warp-collective: every branch around them is warp-uniform
-      ok = __all_sync(0xffffffffu, tc::mbar_wait(bar(B_SFULL + i), j & 1, wait_ns, s_abort));
+      ok = __all_sync(0xffffffffu, tc::mbar_wait_cluster(bar(B_SFULL + i), j & 1, wait_ns, s_abort));
       if (!ok) break;
       tc::tc_fence_after();
       // the whole 128-score row in one TMEM round trip
@@ -447,11 +501,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
       l += ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
       tc::tmem_wait_st();
       tc::tc_fence_before();
-      tc::mbar_arrive(bar(B_PFULL + i));
+      __syncwarp();
+      tc::mbar_arrive_cluster_if(bar_even(B_PFULL + i), lane == 0);
     }
     if (!ok) set_status(p.status, SKV_DEV_TIMEOUT);
     bool done = ok && nt > 0;
-    if (done) done = __all_sync(0xffffffffu, tc::mbar_wait(bar(B_ODONE + i), (nt - 1) & 1, wait_ns, s_abort));
+    if (done) done = __all_sync(0xffffffffu, tc::mbar_wait_cluster(bar(B_ODONE + i), (nt - 1) & 1, wait_ns, s_abort));
     if (done) {
       tc::tc_fence_after();
       const float inv_l = 1.f / l;
@@ -481,11 +536,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
     }
   }
 
+  // no cross-CTA traffic (arrivals, pair MMAs into this CTA's TMEM) after this point
   tc::tc_fence_before();
   __syncthreads();
-  if (warp == WARP_TMA) {
+  tc::cluster_sync();
+  if (warp == WARP_KTMA) {
     tc::tc_fence_after();
-    tc::tmem_dealloc(tmem, 512);
+    tc::tmem_dealloc_pair(tmem, 512);
   }
 }
 
@@ -518,10 +575,10 @@ cudaError_t set_smem_once(K kernel, int bytes, int variant) {
 }  // namespace
 
 // K: [C*Hkv][row_cap][d] -> boxes of 64 dims x k_box_rows rows; V^T:
-// [C*Hkv][d][row_cap] -> boxes of 64 keys x d rows.  Both with the 128-byte
-// swizzle.
-cudaError_t make_kv_tmaps(const Geom& g, const void* k, const void* vt, int k_box_rows, CUtensorMap* tk,
-                          CUtensorMap* tv) {
+// [C*Hkv][d][row_cap] -> boxes of 64 keys x v_box_rows dimension rows.  Both
+// with the 128-byte swizzle.
+cudaError_t make_kv_tmaps(const Geom& g, const void* k, const void* vt, int k_box_rows, int v_box_rows,
+                          CUtensorMap* tk, CUtensorMap* tv) {
   auto fn = encode_fn();
   if (!fn) return cudaErrorNotSupported;
   const cuuint64_t planes = (cuuint64_t)g.C * g.Hkv;
@@ -538,7 +595,7 @@ cudaError_t make_kv_tmaps(const Geom& g, const void* k, const void* vt, int k_bo
   {
     cuuint64_t dims[3] = {(cuuint64_t)g.row_cap, (cuuint64_t)g.d, planes};
     cuuint64_t strides[2] = {(cuuint64_t)g.row_cap * 2, (cuuint64_t)g.row_cap * g.d * 2};
-    cuuint32_t box[3] = {64, (cuuint32_t)g.d, 1};
+    cuuint32_t box[3] = {64, (cuuint32_t)v_box_rows, 1};
     cuuint32_t es[3] = {1, 1, 1};
     if (fn(tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(vt), dims, strides, box, es,
            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -551,16 +608,16 @@ cudaError_t make_kv_tmaps(const Geom& g, const void* k, const void* vt, int k_bo
 cudaError_t launch_prefill_tc(const Geom& g, int Hq, const void* q, void* out, float* lse, const void* k,
                               const void* vt, const float* rope, const int32_t* head, float sm_scale,
                               int32_t* status, uint64_t wait_ns, cudaStream_t st) {
-  if ((g.row_cap + BN - 1) / BN > MAX_TILES) return cudaErrorInvalidValue;
+  if ((g.row_cap + BN - 1) / BN > MAX_TILES || g.V > MAX_VIEWS) return cudaErrorNotSupported;
   CUtensorMap tk, tv;
-  cudaError_t e = make_kv_tmaps(g, k, vt, BN, &tk, &tv);
+  cudaError_t e = make_kv_tmaps(g, k, vt, HN, g.d / 2, &tk, &tv);
   if (e != cudaSuccess) return e;
   PrefillParams p;
   p.g = g;
   p.Hq = Hq;
   p.G = Hq / g.Hkv;
   p.TQ = BM / p.G;
-  p.chunks = (g.T + 2 * p.TQ - 1) / (2 * p.TQ);
+  p.pairs = (g.T + 4 * p.TQ - 1) / (4 * p.TQ);
   p.q = static_cast<const uint16_t*>(q);
   p.out = static_cast<uint16_t*>(out);
   p.lse = lse;
@@ -569,7 +626,7 @@ cudaError_t launch_prefill_tc(const Geom& g, int Hq, const void* q, void* out, f
   p.status = status;
   p.scale_log2 = sm_scale * 1.4426950408889634f;
   p.wait_ns = wait_ns ? wait_ns : 2000000000ull;
-  const long long blocks = (long long)g.C * g.Hkv * g.V * p.chunks;
+  const long long blocks = 2LL * g.C * g.Hkv * g.V * p.pairs;
   if (blocks <= 0) return cudaSuccess;
   if (blocks > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
   if (g.d == 128) {

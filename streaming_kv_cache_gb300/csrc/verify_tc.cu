@@ -177,9 +177,10 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
 
   if (tid == 0) {
     for (int i = 0; i < L::NBAR; ++i) {
+      // warp-wide events arrive once per warp (after __syncwarp)
       const bool many = i == V_QFULL || i == V_KROT || i == V_KROT + 1;
       const bool soft = i == V_PFULL || i == V_PFULL + 1;
-      tc::mbar_init(bar(i), many ? 128 : soft ? SOFTMAX_THREADS : 1);
+      tc::mbar_init(bar(i), many ? 4 : soft ? SOFTMAX_THREADS / 32 : 1);
     }
     *s_abort = 0;
     int ok = 1;
@@ -312,7 +313,8 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
       });
     }
     tc::fence_proxy_async_smem();
-    tc::mbar_arrive(bar(V_QFULL));
+    __syncwarp();
+    if (lane == 0) tc::mbar_arrive(bar(V_QFULL));
     // key tiles: chunk ch (8 frequencies) of NPT consecutive rows per thread
     constexpr int NCH = HALF / 8;
     constexpr int NPT = BN * NCH / 128;   // rows per thread
@@ -378,7 +380,8 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
       }
       if (j + 1 < nt) fetch(j + 1);
       tc::fence_proxy_async_smem();
-      tc::mbar_arrive(bar(V_KROT + s));
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(bar(V_KROT + s));
     }
   } else {
     // ------------------------------------------------- softmax + epilogue
@@ -459,7 +462,8 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
       l += ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
       tc::tmem_wait_st();
       tc::tc_fence_before();
-      tc::mbar_arrive(bar(V_PFULL + sb));
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(bar(V_PFULL + sb));
     }
     if (!ok) set_status(p.status, SKV_DEV_TIMEOUT);
     bool done = ok && nt > 0;
@@ -602,8 +606,8 @@ size_t verify_ws_bytes(const Geom& g, int Hq, int blk) {
   return (units * 4 + 255) / 256 * 256 + rows * (g.d + 2) * sizeof(float);
 }
 
-cudaError_t make_kv_tmaps(const Geom& g, const void* k, const void* vt, int k_box_rows, CUtensorMap* tk,
-                          CUtensorMap* tv);
+cudaError_t make_kv_tmaps(const Geom& g, const void* k, const void* vt, int k_box_rows, int v_box_rows,
+                          CUtensorMap* tk, CUtensorMap* tv);
 
 cudaError_t launch_verify_tc(const Geom& g, int Hq, int blk, const int32_t* tail_len, const void* q, void* out,
                              const void* k, const void* vt, const float* rope, const int32_t* head,
@@ -611,7 +615,7 @@ cudaError_t launch_verify_tc(const Geom& g, int Hq, int blk, const int32_t* tail
                              cudaStream_t st) {
   if (g.V > MAX_VIEWS) return cudaErrorNotSupported;
   CUtensorMap tk, tv;
-  cudaError_t e = make_kv_tmaps(g, k, vt, BN, &tk, &tv);
+  cudaError_t e = make_kv_tmaps(g, k, vt, BN, g.d, &tk, &tv);
   if (e != cudaSuccess) return e;
   VerifyParams p;
   p.g = g;
