@@ -412,13 +412,14 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         for (int k = 0; k < BN; ++k)
           if (r0 + k > lim) v[k] = __float_as_uint(-INFINITY);
       }
-      float m8[8];
+      // row max: four chains of three-input maxima
+      float m4[4];
 #pragma unroll
-      for (int q = 0; q < 8; ++q) m8[q] = __uint_as_float(v[q]);
+      for (int q = 0; q < 4; ++q) m4[q] = fmaxf(__uint_as_float(v[2 * q]), __uint_as_float(v[2 * q + 1]));
 #pragma unroll
-      for (int k = 8; k < BN; ++k) m8[k & 7] = fmaxf(m8[k & 7], __uint_as_float(v[k]));
-      float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                       fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+      for (int k = 8; k < BN; k += 2)
+        m4[(k >> 1) & 3] = fmax3(m4[(k >> 1) & 3], __uint_as_float(v[k]), __uint_as_float(v[k + 1]));
+      float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
       mx *= sl;
       const bool grow = j > 0 && mx > m_used + RESCALE_THRESHOLD;
       if (j == 0) {
@@ -443,7 +444,8 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         tc::tmem_wait_st();
         m_used = m_new;
       }
-      const float nm = -m_used;
+      // scale-and-shift runs on packed fp32 pairs
+      const uint64_t sl2 = f2_pack(sl, sl), nm2 = f2_pack(-m_used, -m_used);
       float l8[8];
 #pragma unroll
       for (int q = 0; q < 8; ++q) l8[q] = 0.f;
@@ -452,8 +454,10 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         uint32_t pk[16];
 #pragma unroll
         for (int k = 0; k < 32; k += 2) {
-          const float p0 = tc::ex2(fmaf(__uint_as_float(v[cb * 32 + k]), sl, nm));
-          const float p1 = tc::ex2(fmaf(__uint_as_float(v[cb * 32 + k + 1]), sl, nm));
+          float x0, x1;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(v[cb * 32 + k]), __uint_as_float(v[cb * 32 + k + 1])), sl2, nm2),
+                    x0, x1);
+          const float p0 = tc::ex2(x0), p1 = tc::ex2(x1);
           l8[(k >> 1) & 7] += p0 + p1;
           pk[k >> 1] = pack_bf16x2(p0, p1);
         }
