@@ -59,6 +59,8 @@ static_assert(256 * REG_SOFTMAX + 128 * REG_CTRL + 128 * REG_ROPE == 65536, "reg
 constexpr int MAX_TILES = 1024;
 constexpr int MAX_VIEWS = 64;
 constexpr float RESCALE_THRESHOLD = 8.0f;
+// pairs of every 16 in a 32-score chunk whose exponentials run on the FMA pipe
+constexpr int FMA_EXP_PAIRS = 0;
 constexpr uint64_t DRAIN_NS = 500000000ull;  // bounded wait for own in-flight copies/MMAs
 
 template <int D>
@@ -239,7 +241,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
             set_status(p.status, SKV_DEV_TIMEOUT);
             break;
           }
-          tc::mbar_arrive_cluster(bar_even(B_VREADY + s));
+          tc::mbar_arrive_cluster_cta_if(bar_even(B_VREADY + s), true);
         }
       }
     } else if (warp == WARP_MMA) {
@@ -404,10 +406,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
           *pb = xb;
         }
       }
-      if (j + 1 < nt) fetch(j + 1);
       tc::fence_proxy_async();
       __syncwarp();
-      tc::mbar_arrive_cluster_if(bar_even(B_KROT + s), lane == 0);
+      tc::mbar_arrive_cluster_cta_if(bar_even(B_KROT + s), lane == 0);
+      // after the arrive, whose release would otherwise wait for these loads
+      if (j + 1 < nt) fetch(j + 1);
     }
   } else {
     // ------------------------------------------------- softmax + epilogue
@@ -495,7 +498,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
           float x0, x1;
           f2_unpack(f2_fma(f2_pack(__uint_as_float(v[cb * 32 + k]), __uint_as_float(v[cb * 32 + k + 1])), sl2, nm2),
                     x0, x1);
-          const float p0 = tc::ex2(x0), p1 = tc::ex2(x1);
+          float p0, p1;
+          if (fma_exp_pair(k >> 1, FMA_EXP_PAIRS)) {
+            exp2_fma_x2(x0, x1, p0, p1);
+          } else {
+            p0 = tc::ex2(x0);
+            p1 = tc::ex2(x1);
+          }
           l8[(k >> 1) & 7] += p0 + p1;
           pk[k >> 1] = pack_bf16x2(p0, p1);
         }
@@ -505,7 +514,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
       tc::tmem_wait_st();
       tc::tc_fence_before();
       __syncwarp();
-      tc::mbar_arrive_cluster_if(bar_even(B_PFULL + i), lane == 0);
+      tc::mbar_arrive_cluster_cta_if(bar_even(B_PFULL + i), lane == 0);
     }
     if (!ok) set_status(p.status, SKV_DEV_TIMEOUT);
     bool done = ok && nt > 0;

@@ -125,6 +125,19 @@ __device__ __forceinline__ void mbar_arrive_cluster_if(uint32_t cluster_addr, bo
       : "memory");
 }
 
+// mbar_arrive_cluster_if with a CTA-scope release: the arrive is ordered
+// after this thread's earlier operations, including a preceding proxy fence
+// (shared-memory data for the pair's tensor core) or tcgen05 fence (data in
+// tensor memory), without the cluster-scope release that stalls the arriving
+// thread for about a thousand cycles while the tensor pipe is busy.
+__device__ __forceinline__ void mbar_arrive_cluster_cta_if(uint32_t cluster_addr, bool pred) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.u32 p, %1, 0;\n"
+      " @p mbarrier.arrive.release.cta.shared::cluster.b64 _, [%0];\n}\n"
+      ::"r"(cluster_addr), "r"((uint32_t)pred)
+      : "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(

@@ -44,6 +44,8 @@ constexpr int SOFTMAX_THREADS = 64;
 constexpr int MAX_VIEWS = 64;
 constexpr int MAX_SPLITS = 64;
 constexpr float RESCALE_THRESHOLD = 8.0f;
+// pairs of every 16 in a 32-score chunk whose exponentials run on the FMA pipe
+constexpr int FMA_EXP_PAIRS = 0;
 constexpr uint64_t DRAIN_NS = 500000000ull;
 
 template <int D>
@@ -457,7 +459,13 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
           float x0, x1;
           f2_unpack(f2_fma(f2_pack(__uint_as_float(v[cb * 32 + k]), __uint_as_float(v[cb * 32 + k + 1])), sl2, nm2),
                     x0, x1);
-          const float p0 = tc::ex2(x0), p1 = tc::ex2(x1);
+          float p0, p1;
+          if (fma_exp_pair(k >> 1, FMA_EXP_PAIRS)) {
+            exp2_fma_x2(x0, x1, p0, p1);
+          } else {
+            p0 = tc::ex2(x0);
+            p1 = tc::ex2(x1);
+          }
           l8[(k >> 1) & 7] += p0 + p1;
           pk[k >> 1] = pack_bf16x2(p0, p1);
         }
