@@ -88,11 +88,10 @@ struct Layout {
 enum {
   B_QFULL = 0,                 // even: 2 x 4 RoPE warps (query tiles rotated)
   B_KFULL = 1,                 // local: this CTA's K half landed (TMA)
-  B_KROT = B_KFULL + NST,      // even: 2 x 4 RoPE warps (K halves rotated)
+  B_KROT = B_KFULL + NST,      // even: 2 x 4 RoPE warps (K halves rotated) + 2 forwarders (V^T halves landed)
   B_KEMPTY = B_KROT + NST,     // pair: K stage free
   B_VFULL = B_KEMPTY + NST,    // local: this CTA's V^T half landed (TMA)
-  B_VREADY = B_VFULL + NST,    // even: 2 forwarders (both V^T halves landed)
-  B_VEMPTY = B_VREADY + NST,   // pair: V stage free
+  B_VEMPTY = B_VFULL + NST,    // pair: V stage free
   B_SFULL = B_VEMPTY + NST,    // pair: S_i ready
   B_PFULL = B_SFULL + 2,       // even: 2 x 4 softmax warps (P_i ready)
   B_ODONE = B_PFULL + 2,       // pair: PV_i issued so far complete
@@ -155,8 +154,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
     for (int i = 0; i < B_COUNT; ++i) {
       // warpgroup-wide events arrive once per warp (after __syncwarp): 2 CTAs x 4 warps
       int count = 1;
-      if (i == B_QFULL || (i >= B_KROT && i < B_KROT + NST) || i == B_PFULL || i == B_PFULL + 1) count = 8;
-      if (i >= B_VREADY && i < B_VREADY + NST) count = 2;
+      if (i == B_QFULL || i == B_PFULL || i == B_PFULL + 1) count = 8;
+      if (i >= B_KROT && i < B_KROT + NST) count = 10;
       tc::mbar_init(bar(i), count);
     }
     *s_abort = 0;
@@ -234,6 +233,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
       }
     } else if (warp == WARP_VFWD) {
       // ------------------- tell the even CTA when this CTA's V^T half landed
+      // (one barrier per stage with the K rotation: a key tile is ready for
+      // both of its MMAs at once, so the MMA issuer waits once per tile)
       if (lane == 0 && nt > 0) {
         for (int j = 0; j < nt; ++j) {
           const int s = j % NST, u = j / NST;
@@ -241,7 +242,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
             set_status(p.status, SKV_DEV_TIMEOUT);
             break;
           }
-          tc::mbar_arrive_cluster_cta_if(bar_even(B_VREADY + s), true);
+          tc::mbar_arrive_cluster_cta_if(bar_even(B_KROT + s), true);
         }
       }
     } else if (warp == WARP_MMA) {
@@ -277,8 +278,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
                             (acc || kk > 0) ? 1u : 0u);
           }
         };
-        bool ok = tc::mbar_wait_cluster(bar(B_QFULL), 0, wait_ns, s_abort);
-        if (ok) ok = tc::mbar_wait_cluster(bar(B_KROT), 0, wait_ns, s_abort);
+        bool ok = tc::mbar_wait_short(bar(B_QFULL), 0, wait_ns, s_abort);
+        if (ok) ok = tc::mbar_wait_short(bar(B_KROT), 0, wait_ns, s_abort);
         if (ok) {
           tc::tc_fence_after();
           issue_qk(0, 0);
@@ -290,18 +291,17 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
         for (int j = 0; ok && j < nt; ++j) {
           const int s = j % NST, u = j / NST;
           const int s2 = (j + 1) % NST, u2 = (j + 1) / NST;
-          if (!(ok = tc::mbar_wait_cluster(bar(B_VREADY + s), u & 1, wait_ns, s_abort))) break;
-          if (!(ok = tc::mbar_wait_cluster(bar(B_PFULL), j & 1, wait_ns, s_abort))) break;
+          if (!(ok = tc::mbar_wait_short(bar(B_PFULL), j & 1, wait_ns, s_abort))) break;
           tc::tc_fence_after();
           issue_pv(0, s, j > 0);
           tc::mma_commit_pair(bar(B_ODONE));
           if (j + 1 < nt) {
-            if (!(ok = tc::mbar_wait_cluster(bar(B_KROT + s2), u2 & 1, wait_ns, s_abort))) break;
+            if (!(ok = tc::mbar_wait_short(bar(B_KROT + s2), u2 & 1, wait_ns, s_abort))) break;
             tc::tc_fence_after();
             issue_qk(0, s2);
             tc::mma_commit_pair(bar(B_SFULL));
           }
-          if (!(ok = tc::mbar_wait_cluster(bar(B_PFULL + 1), j & 1, wait_ns, s_abort))) break;
+          if (!(ok = tc::mbar_wait_short(bar(B_PFULL + 1), j & 1, wait_ns, s_abort))) break;
           tc::tc_fence_after();
           issue_pv(1, s, j > 0);
           tc::mma_commit_pair(bar(B_ODONE + 1));

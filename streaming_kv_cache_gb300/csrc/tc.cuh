@@ -53,17 +53,32 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Wait for the phase with the given parity to complete.  The wait is bounded:
-// after limit_ns nanoseconds (counted in SM cycles at the 2.07 GHz maximum
-// clock, so a slower clock only lengthens it) it raises *abort and returns
-// false; it also returns false once another thread has raised *abort.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns,
-                                          volatile int* abort) {
-  if (mbar_try_wait(bar, parity)) return true;
+// try_wait without a suspend-time hint: the hardware's own short time limit,
+// then the caller polls again.  A waiter on the critical path resumes sooner
+// after the phase completes than one suspended with a long hint.
+__device__ __forceinline__ bool mbar_try_wait_short(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Poll try(bar, parity) until it succeeds.  The wait is bounded: after
+// limit_ns nanoseconds (counted in SM cycles at the 2.07 GHz maximum clock,
+// so a slower clock only lengthens it) it raises *abort and returns false; it
+// also returns false once another thread has raised *abort.
+template <typename Try>
+__device__ __forceinline__ bool bounded_wait(Try try_fn, uint32_t bar, uint32_t parity, uint64_t limit_ns,
+                                             volatile int* abort) {
+  if (try_fn(bar, parity)) return true;
   const long long limit = (long long)(limit_ns * 2.07);
   const long long t0 = clock64();
   for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (try_fn(bar, parity)) return true;
     if ((it & 63) == 0) {
       if (*abort) return false;
       if (clock64() - t0 > limit) {
@@ -72,6 +87,18 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_
       }
     }
   }
+}
+
+// Wait for the phase with the given parity to complete (bounded, see bounded_wait).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns,
+                                          volatile int* abort) {
+  return bounded_wait(mbar_try_wait, bar, parity, limit_ns, abort);
+}
+
+// The same with short polls, for the MMA issuer.
+__device__ __forceinline__ bool mbar_wait_short(uint32_t bar, uint32_t parity, uint64_t limit_ns,
+                                                volatile int* abort) {
+  return bounded_wait(mbar_try_wait_short, bar, parity, limit_ns, abort);
 }
 
 // A value the compiler must (re)compute where it stands: keeps loop-invariant
@@ -153,19 +180,7 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
 // receive arrivals from the peer CTA or from a pair MMA's commit.
 __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, uint64_t limit_ns,
                                                   volatile int* abort) {
-  if (mbar_try_wait_cluster(bar, parity)) return true;
-  const long long limit = (long long)(limit_ns * 2.07);
-  const long long t0 = clock64();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait_cluster(bar, parity)) return true;
-    if ((it & 63) == 0) {
-      if (*abort) return false;
-      if (clock64() - t0 > limit) {
-        *abort = 1;
-        return false;
-      }
-    }
-  }
+  return bounded_wait(mbar_try_wait_cluster, bar, parity, limit_ns, abort);
 }
 
 __device__ __forceinline__ void cluster_sync() {
