@@ -86,8 +86,9 @@ struct Layout {
 // barrier slots.  "even" = lives in the even CTA only and counts the
 // arrivals of both CTAs; "pair" = completed by a pair-MMA commit in both.
 enum {
-  B_QFULL = 0,                 // even: 2 x 4 RoPE warps (query tiles rotated)
-  B_KFULL = 1,                 // local: this CTA's K half landed (TMA)
+  B_QFULL = 0,                 // even: 2 x 8 softmax warps (query tiles rotated)
+  B_QLOAD = 1,                 // local: this CTA's query tiles landed (TMA)
+  B_KFULL = 2,                 // local: this CTA's K half landed (TMA)
   B_KROT = B_KFULL + NST,      // even: 2 x 4 RoPE warps (K halves rotated) + 2 forwarders (V^T halves landed)
   B_KEMPTY = B_KROT + NST,     // pair: K stage free
   B_VFULL = B_KEMPTY + NST,    // local: this CTA's V^T half landed (TMA)
@@ -116,7 +117,7 @@ struct PrefillParams {
 template <int D>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
-                  const PrefillParams p) {
+                  const __grid_constant__ CUtensorMap tmap_q, const PrefillParams p) {
   using L = Layout<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -150,38 +151,48 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
   const int zc = c * g.Hkv + h;                    // (cache, kv head) plane of the tensor maps
   const uint64_t wait_ns = p.wait_ns;
 
-  if (tid == 0) {
-    for (int i = 0; i < B_COUNT; ++i) {
-      // warpgroup-wide events arrive once per warp (after __syncwarp): 2 CTAs x 4 warps
-      int count = 1;
-      if (i == B_QFULL || i == B_PFULL || i == B_PFULL + 1) count = 8;
-      if (i >= B_KROT && i < B_KROT + NST) count = 10;
-      tc::mbar_init(bar(i), count);
+  if (warp == 0) {
+    if (lane == 0) {
+      for (int i = 0; i < B_COUNT; ++i) {
+        // warpgroup-wide events arrive once per warp (after __syncwarp)
+        int count = 1;
+        if (i == B_PFULL || i == B_PFULL + 1) count = 8;      // 2 CTAs x 4 warps
+        if (i >= B_KROT && i < B_KROT + NST) count = 10;      // 2 x 4 RoPE warps + 2 forwarders
+        if (i == B_QFULL) count = 16;                         // 2 CTAs x 8 softmax warps
+        tc::mbar_init(bar(i), count);
+      }
+      *s_abort = 0;
     }
-    *s_abort = 0;
-    // tile list over physical key rows [0, row_end), skipping tiles made only
-    // of newest-frame rows that no query of the pair may see
-    int ok = 1;
-    for (int v = 0; v <= vq; ++v) {
+    // ring heads of views 0..vq, one lane per view
+    bool ok = true;
+    for (int v = lane; v <= vq; v += 32) {
       const int hv = head_c[v];
-      if (hv < 0 || hv >= g.F) ok = 0;
+      ok = ok && hv >= 0 && hv < g.F;
       s_head[v] = hv;
     }
+    ok = __all_sync(0xffffffffu, ok);
+    // tile list over physical key rows [0, row_end), skipping tiles made only
+    // of newest-frame rows that no query of the pair may see; 32 tiles per step
     int n = 0;
     if (ok) {
       const int s_new = (head_c[vq] + g.F - 1) % g.F;
       const int ns0 = g.P + (vq * g.F + s_new) * g.T;
       const int inv_lo = ns0 + t_max + 1, inv_hi = ns0 + g.T;
-      for (int r0 = 0; r0 < row_end && n < MAX_TILES; r0 += BN) {
-        const int r1 = min(r0 + BN, row_end);
-        if (r0 >= inv_lo && r1 <= inv_hi) continue;
-        s_tiles[n++] = r0;
+      const int n_all = (row_end + BN - 1) / BN;
+      for (int k0 = 0; k0 < n_all; k0 += 32) {
+        const int k = k0 + lane, r0 = k * BN;
+        const bool keep = k < n_all && !(r0 >= inv_lo && min(r0 + BN, row_end) <= inv_hi);
+        const uint32_t ball = __ballot_sync(0xffffffffu, keep);
+        if (keep) s_tiles[n + __popc(ball & ((1u << lane) - 1))] = r0;
+        n += __popc(ball);
       }
-    } else if (rank == 0) {
+    } else if (rank == 0 && lane == 0) {
       set_status(p.status, SKV_DEV_BAD_HEAD);
     }
-    *s_ntiles = n;
-    tc::fence_barrier_init();
+    if (lane == 0) {
+      *s_ntiles = n;
+      tc::fence_barrier_init();
+    }
   }
   if (warp == WARP_KTMA) {
     tc::tmem_alloc_pair(tc::smem_u32(s_tmem), 512);
@@ -201,6 +212,17 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
       const bool is_k = warp == WARP_KTMA;
       if (lane == 0 && nt > 0) {
         tc::prefetch_tmap(is_k ? &tmap_k : &tmap_v);
+        if (is_k) {
+          // both query tiles: rows (token, head) of kv head h, 64 columns per box
+          const int z0 = (c * g.V + vq) * g.T + t0;
+          tc::mbar_arrive_expect_tx(bar(B_QLOAD), 2 * L::QT);
+#pragma unroll
+          for (int i = 0; i < 2; ++i)
+#pragma unroll
+            for (int hf = 0; hf < D / 64; ++hf)
+              tc::tma_load_3d(sbase + L::Q_OFF + i * L::QT + hf * L::HALF_Q, &tmap_q, bar(B_QLOAD), hf * 64,
+                              h * p.G, z0 + i * p.TQ);
+        }
         int issued = 0;
         for (int j = 0; j < nt; ++j) {
           const int s = j % NST, u = j / NST, r0 = s_tiles[j];
@@ -225,6 +247,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
         if (*s_abort) {
           set_status(p.status, SKV_DEV_TIMEOUT);
           // let the copies this thread started land before the CTA exits
+          if (is_k) {
+            volatile int never = 0;
+            tc::mbar_wait(bar(B_QLOAD), 0, DRAIN_NS, &never);
+          }
           for (int j = max(0, issued - NST); j < issued; ++j) {
             volatile int never = 0;
             tc::mbar_wait(bar((is_k ? B_KFULL : B_VFULL) + j % NST), (j / NST) & 1, DRAIN_NS, &never);
@@ -289,7 +315,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
           tc::mma_commit_pair(bar(B_KEMPTY));
         }
         for (int j = 0; ok && j < nt; ++j) {
-          const int s = j % NST, u = j / NST;
+          const int s = j % NST;
           const int s2 = (j + 1) % NST, u2 = (j + 1) / NST;
           if (!(ok = tc::mbar_wait_short(bar(B_PFULL), j & 1, wait_ns, s_abort))) break;
           tc::tc_fence_after();
@@ -326,18 +352,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
     tc::setmaxnreg_dec<REG_ROPE>();
     const int rt = tid - WARP_ROPE * 32;   // 0..127
     constexpr int HALF = D / 2;
-    // query tiles: row r of tile i = (token t0 + i*TQ + r/G, head r%G), rotated
-    // at its logical position (fp16, swizzled K-major)
-    load_rotate_q<D>(smem + L::Q_OFF, 2, L::QT, L::HALF_Q, p.rope, rt, [&](int rr, int& pos) -> const uint16_t* {
-      const int i = rr / 128, r = rr % 128;
-      const int tok = t0 + i * p.TQ + r / p.G;
-      pos = g.P + vq * FT + (g.F - 1) * g.T + min(tok, g.T - 1);
-      if (tok >= g.T) return nullptr;
-      return p.q + (((size_t)c * (g.V * g.T) + vq * g.T + tok) * p.Hq + h * p.G + r % p.G) * D;
-    });
-    tc::fence_proxy_async();
-    __syncwarp();
-    tc::mbar_arrive_cluster_if(bar_even(B_QFULL), lane == 0);
     // this CTA's 64 rows of every key tile, rotated in place once TMA has
     // landed them.  Thread (warp wr, lane ln) takes chunk ch = ln % NCH (8
     // frequencies) of NPT consecutive rows; inside a frame consecutive rows
@@ -433,8 +447,50 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
     const float sl = p.scale_log2;
     float m_used = -INFINITY, l = 0.f;
     bool ok = true;
+    if (nt > 0) {
+      // query tiles as TMA landed them: bf16 row r of tile qi = (token
+      // t0 + qi*TQ + r/G, head r%G); rotate in place, at each token's
+      // logical position, into fp16.  Thread tid takes chunk ch (8
+      // frequencies) of NCH consecutive rows, four rows at a time.
+      ok = __all_sync(0xffffffffu, tc::mbar_wait(bar(B_QLOAD), 0, wait_ns, s_abort));
+      if (ok) {
+        constexpr int HALF = D / 2, NCH = HALF / 8;
+        const int ch = tid % NCH, rr0 = (tid / NCH) * NCH;
+        const int ea = ch * 8, eb = HALF + ch * 8;
+        const uint32_t off_a = (ea / 64) * L::HALF_Q, off_b = (eb / 64) * L::HALF_Q;
+        const int ca = (ea % 64) / 8, cb = (eb % 64) / 8;
+        const float4* rope4 = reinterpret_cast<const float4*>(p.rope);
+        const int pos_base = g.P + vq * FT + (g.F - 1) * g.T;
+#pragma unroll
+        for (int b4 = 0; b4 < NCH; b4 += 4) {
+          uint4 xa[4], xb[4];
+          float4 cs[4][4];
+          uint8_t* rp[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int rr = rr0 + b4 + q, qi = rr >> 7, r = rr & 127;
+            const int qtok = min(t0 + qi * p.TQ + r / p.G, g.T - 1);
+            rp[q] = smem + L::Q_OFF + qi * L::QT;
+            xa[q] = *reinterpret_cast<const uint4*>(rp[q] + off_a + tc::sw128_off(r, ca));
+            xb[q] = *reinterpret_cast<const uint4*>(rp[q] + off_b + tc::sw128_off(r, cb));
+#pragma unroll
+            for (int w4 = 0; w4 < 4; ++w4) cs[q][w4] = __ldg(rope4 + ((size_t)(pos_base + qtok) * HALF + ea) / 2 + w4);
+          }
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int r = (rr0 + b4 + q) & 127;
+            rotate_pairs4(xa[q], xb[q], cs[q]);
+            *reinterpret_cast<uint4*>(rp[q] + off_a + tc::sw128_off(r, ca)) = xa[q];
+            *reinterpret_cast<uint4*>(rp[q] + off_b + tc::sw128_off(r, cb)) = xb[q];
+          }
+        }
+        tc::fence_proxy_async();
+      }
+      __syncwarp();
+      tc::mbar_arrive_cluster_cta_if(bar_even(B_QFULL), lane == 0 && ok);
+    }
 #pragma unroll 1
-    for (int j = 0; j < nt; ++j) {
+    for (int j = 0; ok && j < nt; ++j) {
       // tcgen05.ld/st below are warp-collective: every branch around them is warp-uniform
       ok = __all_sync(0xffffffffu, tc::mbar_wait_cluster(bar(B_SFULL + i), j & 1, wait_ns, s_abort));
       if (!ok) break;
@@ -621,9 +677,24 @@ cudaError_t launch_prefill_tc(const Geom& g, int Hq, const void* q, void* out, f
                               const void* vt, const float* rope, const int32_t* head, float sm_scale,
                               int32_t* status, uint64_t wait_ns, cudaStream_t st) {
   if ((g.row_cap + BN - 1) / BN > MAX_TILES || g.V > MAX_VIEWS) return cudaErrorNotSupported;
-  CUtensorMap tk, tv;
+  CUtensorMap tk, tv, tq;
   cudaError_t e = make_kv_tmaps(g, k, vt, HN, g.d / 2, &tk, &tv);
   if (e != cudaSuccess) return e;
+  {
+    // queries [C * V * T tokens][Hq][d] bf16: a box is 64 columns of the G
+    // heads of one kv head for TQ tokens, i.e. 128 rows (token, head) of 128 B
+    const int G = Hq / g.Hkv;
+    cuuint64_t dims[3] = {(cuuint64_t)g.d, (cuuint64_t)Hq, (cuuint64_t)g.C * g.V * g.T};
+    cuuint64_t strides[2] = {(cuuint64_t)g.d * 2, (cuuint64_t)Hq * g.d * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)G, (cuuint32_t)(BM / G)};
+    cuuint32_t es[3] = {1, 1, 1};
+    auto fn = encode_fn();
+    if (!fn) return cudaErrorNotSupported;
+    if (fn(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides, box, es,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
   PrefillParams p;
   p.g = g;
   p.Hq = Hq;
@@ -644,11 +715,11 @@ cudaError_t launch_prefill_tc(const Geom& g, int Hq, const void* q, void* out, f
   if (g.d == 128) {
     const int smem = Layout<128>::ALLOC;
     if ((e = set_smem_once(prefill_tc_kernel<128>, smem, 0)) != cudaSuccess) return e;
-    prefill_tc_kernel<128><<<(unsigned)blocks, NTHREADS, smem, st>>>(tk, tv, p);
+    prefill_tc_kernel<128><<<(unsigned)blocks, NTHREADS, smem, st>>>(tk, tv, tq, p);
   } else {
     const int smem = Layout<64>::ALLOC;
     if ((e = set_smem_once(prefill_tc_kernel<64>, smem, 1)) != cudaSuccess) return e;
-    prefill_tc_kernel<64><<<(unsigned)blocks, NTHREADS, smem, st>>>(tk, tv, p);
+    prefill_tc_kernel<64><<<(unsigned)blocks, NTHREADS, smem, st>>>(tk, tv, tq, p);
   }
   return cudaGetLastError();
 }
