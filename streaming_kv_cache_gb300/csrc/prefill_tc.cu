@@ -368,9 +368,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
     const uint32_t off_a = (ea / 64) * L::HALF_K, off_b = (eb / 64) * L::HALF_K;
     const int ca = (ea % 64) / 8, cb = (eb % 64) / 8;
     const float4* rope4 = reinterpret_cast<const float4*>(p.rope);
-    float4 step[4];
+    float4 step4[4];
 #pragma unroll
-    for (int w4 = 0; w4 < 4; ++w4) step[w4] = __ldg(rope4 + (HALF + ea) / 2 + w4);   // R(1)
+    for (int w4 = 0; w4 < 4; ++w4) step4[w4] = __ldg(rope4 + (HALF + ea) / 2 + w4);   // R(1)
+    const Ang8 step = ang8_from(step4);
     const int row0 = HN * (int)rank + row_base;       // this thread's first row inside a tile
     int pf_pos = -1, pf_run = 0;
     float4 pf[4];
@@ -391,35 +392,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
         set_status(p.status, SKV_DEV_TIMEOUT);
         break;
       }
-      if (pf_pos >= 0) {
-        uint8_t* kt = smem + L::K_OFF + s * L::KST;
-        const int r0 = s_tiles[j] + row0;
-        int pos = pf_pos, run = pf_run;
-        float4 cs[4] = {pf[0], pf[1], pf[2], pf[3]};
-#pragma unroll
-        for (int k = 0; k < NPT; ++k) {
-          const int r = r0 + k;
-          if (r >= row_end) break;
-          if (k > 0) {
-            if (run > 1) {
-              --run;
-              ++pos;
-              advance_angles(cs, step);
-            } else {
-              key_pos_run(g, s_head, r, pos, run);
-#pragma unroll
-              for (int w4 = 0; w4 < 4; ++w4) cs[w4] = __ldg(rope4 + ((size_t)pos * HALF + ea) / 2 + w4);
-            }
-          }
-          const int row = row_base + k;
-          uint4* pa = reinterpret_cast<uint4*>(kt + off_a + tc::sw128_off(row, ca));
-          uint4* pb = reinterpret_cast<uint4*>(kt + off_b + tc::sw128_off(row, cb));
-          uint4 xa = *pa, xb = *pb;
-          rotate_pairs4(xa, xb, cs);
-          *pa = xa;
-          *pb = xb;
-        }
-      }
+      if (pf_pos >= 0)
+        rotate_key_rows<NPT>(smem + L::K_OFF + s * L::KST, off_a, off_b, ca, cb, row_base, s_tiles[j] + row0,
+                             row_end, pf_pos, pf_run, pf, step, g, s_head, rope4, ea, HALF);
       tc::fence_proxy_async();
       __syncwarp();
       tc::mbar_arrive_cluster_cta_if(bar_even(B_KROT + s), lane == 0);
@@ -614,19 +589,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
   }
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-  }
-  return fn;
-}
-
 // Raise the kernel's dynamic shared-memory limit once per device.
 template <typename K>
 cudaError_t set_smem_once(K kernel, int bytes, int variant) {
@@ -645,9 +607,23 @@ cudaError_t set_smem_once(K kernel, int bytes, int variant) {
 // K: [C*Hkv][row_cap][d] -> boxes of 64 dims x k_box_rows rows; V^T:
 // [C*Hkv][d][row_cap] -> boxes of 64 keys x v_box_rows dimension rows.  Both
 // with the 128-byte swizzle.
+// cuTensorMapEncodeTiled from the driver, looked up once (no link against libcuda).
+PFN_cuTensorMapEncodeTiled_v12000 tmap_encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
 cudaError_t make_kv_tmaps(const Geom& g, const void* k, const void* vt, int k_box_rows, int v_box_rows,
                           CUtensorMap* tk, CUtensorMap* tv) {
-  auto fn = encode_fn();
+  auto fn = tmap_encode_fn();
   if (!fn) return cudaErrorNotSupported;
   const cuuint64_t planes = (cuuint64_t)g.C * g.Hkv;
   {
@@ -688,7 +664,7 @@ cudaError_t launch_prefill_tc(const Geom& g, int Hq, const void* q, void* out, f
     cuuint64_t strides[2] = {(cuuint64_t)g.d * 2, (cuuint64_t)Hq * g.d * 2};
     cuuint32_t box[3] = {64, (cuuint32_t)G, (cuuint32_t)(BM / G)};
     cuuint32_t es[3] = {1, 1, 1};
-    auto fn = encode_fn();
+    auto fn = tmap_encode_fn();
     if (!fn) return cudaErrorNotSupported;
     if (fn(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides, box, es,
            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,

@@ -1,6 +1,7 @@
 // Device helpers shared by the attention kernels for the rotary embedding
 // applied on the fly: rotate-half rotation of bf16 pairs into fp16, logical
-// positions of physical key rows, and the angle step R(p+1) = R(p) R(1).
+// positions of physical key rows, the angle step R(p+1) = R(p) R(1), and the
+// in-place rotation of a thread's rows of a key tile.
 //
 // FlashDrive blog walkthrough, section 3.3 "RoPE Position Shift": keys are
 // cached without rotation and rotated at their current logical position.
@@ -9,6 +10,7 @@
 #include <stdint.h>
 
 #include "common.cuh"
+#include "tc.cuh"
 
 namespace skv {
 
@@ -27,14 +29,6 @@ __device__ __forceinline__ void rotate_pairs4(uint4& a, uint4& b, const float4 (
     pa[w] = pack_f16x2_sat(x0 * t[w].x - y0 * t[w].y, x1 * t[w].z - y1 * t[w].w);
     pb[w] = pack_f16x2_sat(y0 * t[w].x + x0 * t[w].y, y1 * t[w].z + x1 * t[w].w);
   }
-}
-
-__device__ __forceinline__ void rotate_pairs(uint4& a, uint4& b, const float2* __restrict__ cs) {
-  const float4* c4 = reinterpret_cast<const float4*>(cs);
-  float4 t[4];
-#pragma unroll
-  for (int w = 0; w < 4; ++w) t[w] = __ldg(c4 + w);
-  rotate_pairs4(a, b, t);
 }
 
 // Logical position of physical key row r and how many rows from r on (r
@@ -64,72 +58,109 @@ __device__ __forceinline__ void key_pos_run(const Geom& g, const int* __restrict
   run = g.T - t;
 }
 
-__device__ __forceinline__ void advance_angles(float4 (&cs)[4], const float4 (&st)[4]) {
+// The (cos, sin) of the 8 frequencies of one chunk as packed fp32 pairs:
+// c[w] = cosines of frequencies 2w and 2w+1, s[w] their sines.
+struct Ang8 {
+  uint64_t c[4], s[4];
+};
+
+// From table entries t[w] = (cos f_2w, sin f_2w, cos f_2w+1, sin f_2w+1).
+__device__ __forceinline__ Ang8 ang8_from(const float4 (&t)[4]) {
+  Ang8 a;
 #pragma unroll
   for (int w = 0; w < 4; ++w) {
-    const float4 c = cs[w];
-    cs[w] = make_float4(c.x * st[w].x - c.y * st[w].y, c.y * st[w].x + c.x * st[w].y,
-                        c.z * st[w].z - c.w * st[w].w, c.w * st[w].z + c.z * st[w].w);
+    a.c[w] = f2_pack(t[w].x, t[w].z);
+    a.s[w] = f2_pack(t[w].y, t[w].w);
+  }
+  return a;
+}
+
+// R(p+1) = R(p) R(1) per frequency: r = R(1) of the chunk.
+__device__ __forceinline__ void ang8_step(Ang8& a, const Ang8& r) {
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    const uint64_t c = a.c[w], s = a.s[w];
+    a.c[w] = f2_sub(f2_mul(c, r.c[w]), f2_mul(s, r.s[w]));
+    a.s[w] = f2_fma(c, r.s[w], f2_mul(s, r.c[w]));
   }
 }
 
-}  // namespace skv
-
-namespace skv {
-
-// Load n_tiles query tiles of 128 rows into shared memory, rotated at their
-// positions and stored as fp16 in the 128-byte-swizzled K-major layout
-// (tile t at dst + t*tile_bytes, 64-column halves half_bytes apart).  The
-// (row, 8-pair chunk) items are spread over the 128 calling threads and
-// fetched two at a time, so the global and table loads overlap.
-// row_src(r) returns the pre-RoPE bf16 row of tile row r (nullptr for a
-// padding row, which is zero-filled) and its position.
-template <int D, typename RowSrc>
-__device__ __forceinline__ void load_rotate_q(uint8_t* dst, int n_tiles, int tile_bytes, int half_bytes,
-                                              const float2* __restrict__ rope, int tid128, RowSrc row_src) {
-  constexpr int HALF = D / 2;
-  constexpr int NCH = HALF / 8;
-  constexpr int BATCH = 2;
-  const int n_items = n_tiles * 128 * NCH;
-  for (int i0 = tid128 * BATCH; i0 < n_items; i0 += 128 * BATCH) {
-    uint4 xa[BATCH], xb[BATCH];
-    float4 t[BATCH][4];
-    int rr[BATCH], cc[BATCH];
-    bool live[BATCH];
+// rotate_pairs4 on packed fp32 pairs: x' = x cos - y sin, y' = y cos + x sin
+// for the 8 (x, y) = (a, b) element pairs, fp16 out clamped to the finite range.
+__device__ __forceinline__ void rotate8(uint4& a, uint4& b, const Ang8& t) {
+  uint32_t* pa = reinterpret_cast<uint32_t*>(&a);
+  uint32_t* pb = reinterpret_cast<uint32_t*>(&b);
 #pragma unroll
-    for (int q = 0; q < BATCH; ++q) {
-      const int it = i0 + q;
-      rr[q] = it / NCH;
-      cc[q] = it % NCH;
-      live[q] = false;
-      if (it < n_items) {
-        int pos;
-        const uint16_t* src = row_src(rr[q], pos);
-        if (src) {
-          live[q] = true;
-          xa[q] = *reinterpret_cast<const uint4*>(src + cc[q] * 8);
-          xb[q] = *reinterpret_cast<const uint4*>(src + HALF + cc[q] * 8);
-          const float4* c4 = reinterpret_cast<const float4*>(rope + (size_t)pos * HALF + cc[q] * 8);
+  for (int w = 0; w < 4; ++w) {
+    const uint64_t x = f2_pack(bf16_lo(pa[w]), bf16_hi(pa[w]));
+    const uint64_t y = f2_pack(bf16_lo(pb[w]), bf16_hi(pb[w]));
+    const uint64_t xr = f2_sub(f2_mul(x, t.c[w]), f2_mul(y, t.s[w]));
+    const uint64_t yr = f2_fma(x, t.s[w], f2_mul(y, t.c[w]));
+    float x0, x1, y0, y1;
+    f2_unpack(xr, x0, x1);
+    f2_unpack(yr, y0, y1);
+    pa[w] = pack_f16x2_sat(x0, x1);
+    pb[w] = pack_f16x2_sat(y0, y1);
+  }
+}
+
+// Rotate rows r0 .. r0+NPT-1 (tile rows row_base ..) of a key tile in shared
+// memory, this thread's 8-frequency chunk (a half at off_a/chunk ca, b half at
+// off_b/chunk cb); rows at or past row_lim are left as they are.  pos/run and
+// first describe row r0 (its logical position, the rows from it on with
+// consecutive positions, its table angles).  Inside one run the angles step
+// by R(1); rows are loaded two at a time before they are rotated.
+template <int NPT>
+__device__ __forceinline__ void rotate_key_rows(uint8_t* kt, uint32_t off_a, uint32_t off_b, int ca, int cb,
+                                                int row_base, int r0, int row_lim, int pos, int run,
+                                                const float4 (&first)[4], const Ang8& step, const Geom& g,
+                                                const int* heads, const float4* rope4, int ea, int half) {
+  if (run >= NPT && r0 + NPT <= row_lim) {
+    // two rows in flight at a time (registers)
+    Ang8 ang = ang8_from(first);
 #pragma unroll
-          for (int w = 0; w < 4; ++w) t[q][w] = __ldg(c4 + w);
-        }
+    for (int k0 = 0; k0 < NPT; k0 += 2) {
+      uint4 xa[2], xb[2];
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        xa[k] = *reinterpret_cast<const uint4*>(kt + off_a + tc::sw128_off(row_base + k0 + k, ca));
+        xb[k] = *reinterpret_cast<const uint4*>(kt + off_b + tc::sw128_off(row_base + k0 + k, cb));
+      }
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        if (k0 + k > 0) ang8_step(ang, step);
+        rotate8(xa[k], xb[k], ang);
+        *reinterpret_cast<uint4*>(kt + off_a + tc::sw128_off(row_base + k0 + k, ca)) = xa[k];
+        *reinterpret_cast<uint4*>(kt + off_b + tc::sw128_off(row_base + k0 + k, cb)) = xb[k];
       }
     }
-#pragma unroll
-    for (int q = 0; q < BATCH; ++q) {
-      if (i0 + q >= n_items) continue;
-      if (live[q]) {
-        rotate_pairs4(xa[q], xb[q], t[q]);
+    return;
+  }
+  // a run boundary or the end of the keys inside this thread's rows
+  Ang8 ang = ang8_from(first);
+#pragma unroll 1
+  for (int k = 0; k < NPT; ++k) {
+    const int r = r0 + k;
+    if (r >= row_lim) break;
+    if (k > 0) {
+      if (run > 1) {
+        --run;
+        ++pos;
+        ang8_step(ang, step);
       } else {
-        xa[q] = make_uint4(0, 0, 0, 0);
-        xb[q] = xa[q];
+        key_pos_run(g, heads, r, pos, run);
+        float4 t[4];
+#pragma unroll
+        for (int w4 = 0; w4 < 4; ++w4) t[w4] = __ldg(rope4 + ((size_t)pos * half + ea) / 2 + w4);
+        ang = ang8_from(t);
       }
-      const int tile = rr[q] / 128, row = rr[q] % 128;
-      const int ea = cc[q] * 8, eb = HALF + cc[q] * 8;
-      uint8_t* base = dst + tile * tile_bytes;
-      *reinterpret_cast<uint4*>(base + (ea / 64) * half_bytes + row * 128 + ((((ea % 64) / 8) ^ (row & 7)) << 4)) = xa[q];
-      *reinterpret_cast<uint4*>(base + (eb / 64) * half_bytes + row * 128 + ((((eb % 64) / 8) ^ (row & 7)) << 4)) = xb[q];
     }
+    uint4* pa = reinterpret_cast<uint4*>(kt + off_a + tc::sw128_off(row_base + k, ca));
+    uint4* pb = reinterpret_cast<uint4*>(kt + off_b + tc::sw128_off(row_base + k, cb));
+    uint4 xa = *pa, xb = *pb;
+    rotate8(xa, xb, ang);
+    *pa = xa;
+    *pb = xb;
   }
 }
 
