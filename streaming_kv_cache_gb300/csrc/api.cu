@@ -185,16 +185,15 @@ int stream_attn_verify(const skv_cache* cache, int32_t n_q_head, int32_t blk,
   if ((rc = check_device())) return rc;
   const skv::Geom g = skv::geom_of(*cache);
   cudaStream_t st = (cudaStream_t)stream;
+  // the block's K/V into the tail, and the accept length from the ids
   cudaError_t e = skv::launch_write_rows(g, cache->k, cache->vt, k_blk, v_blk, 1, blk, 2, 0,
-                                         cache->head, cache->sync, tail_len, cache->status, st);
+                                         cache->head, cache->sync, tail_len, cache->status, st,
+                                         ids ? target_ids : nullptr, ids ? draft_ids : nullptr,
+                                         ids ? accept_len : nullptr, ids ? next_token : nullptr);
   if (e != cudaSuccess) return cuda_fail(e);
   e = skv::launch_verify_tc(g, n_q_head, blk, tail_len, q_blk, out, cache->k, cache->vt, cache->rope,
                             cache->head, ws, ws_bytes, sm_scale, cache->status, cache->wait_ns, st);
   if (e != cudaSuccess) return cuda_fail(e);
-  if (ids) {
-    e = skv::launch_accept(g.C, blk, target_ids, draft_ids, accept_len, next_token, st);
-    if (e != cudaSuccess) return cuda_fail(e);
-  }
   return SKV_OK;
 }
 

@@ -11,6 +11,10 @@
 // rows are straight 16-byte copies into [row][d]; the V rows go through
 // shared memory and are written transposed into [d][row], one coalesced run
 // of CH tokens per dimension.
+//
+// The verify block's tail write also computes the greedy accept length (it
+// needs only the token ids) and lets the attention kernel that follows launch
+// early: that kernel waits for this one's writes only before it reads tail rows.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -23,14 +27,24 @@ constexpr int THREADS = 128;
 
 enum WriteMode { MODE_ROWS = 0, MODE_INSERT = 1, MODE_TAIL = 2 };
 
+// Token ids of a verify block and the accept outputs (all null: none).
+struct AcceptArgs {
+  const int32_t* target;
+  const int32_t* draft;
+  int32_t* accept_len;
+  int32_t* next_token;
+};
+
 template <int D>
 __global__ void __launch_bounds__(THREADS) write_rows_kernel(
     Geom g, uint16_t* __restrict__ k, uint16_t* __restrict__ vt,
     const uint16_t* __restrict__ k_src, const uint16_t* __restrict__ v_src, int n_group,
     int n_tok, int mode, int row0, int32_t* __restrict__ head, int32_t* __restrict__ sync,
-    const int32_t* __restrict__ tail_len, int32_t* __restrict__ status) {
+    const int32_t* __restrict__ tail_len, int32_t* __restrict__ status, AcceptArgs acc) {
   __shared__ __align__(16) uint16_t sv[CH][D + 2];
   __shared__ int s_base;
+  // the attention kernel after a tail write may start its own set-up now
+  if (mode == MODE_TAIL) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   const int n_chunk = (n_tok + CH - 1) / CH;
   int bid = blockIdx.x;
@@ -89,6 +103,17 @@ __global__ void __launch_bounds__(THREADS) write_rows_kernel(
     }
   }
 
+  if (mode == MODE_TAIL && acc.target && h == 0 && chunk == 0 && threadIdx.x == 0) {
+    // greedy longest prefix: the largest k <= n_tok-1 with draft[i] == target[i-1]
+    // for 1 <= i <= k; the target's own token at k comes next
+    const int32_t* t = acc.target + (size_t)c * n_tok;
+    const int32_t* dr = acc.draft + (size_t)c * n_tok;
+    int kk = 0;
+    while (kk + 1 < n_tok && dr[kk + 1] == t[kk]) ++kk;
+    acc.accept_len[c] = kk;
+    acc.next_token[c] = t[kk];
+  }
+
   if (mode == MODE_INSERT) {
     // The last CTA of this (cache, view) to finish advances the head; every
     // CTA has read the head before it arrives here, and the counter is left
@@ -112,7 +137,9 @@ __global__ void __launch_bounds__(THREADS) write_rows_kernel(
 cudaError_t launch_write_rows(const Geom& g, void* k, void* vt, const void* k_src,
                               const void* v_src, int n_group, int n_tok, int mode, int row0,
                               int32_t* head, int32_t* sync, const int32_t* tail_len,
-                              int32_t* status, cudaStream_t st) {
+                              int32_t* status, cudaStream_t st, const int32_t* target,
+                              const int32_t* draft, int32_t* accept_len, int32_t* next_token) {
+  const AcceptArgs acc{target, draft, accept_len, next_token};
   if (n_tok <= 0 || g.C <= 0) return cudaSuccess;
   const long long blocks = (long long)g.C * n_group * g.Hkv * ((n_tok + CH - 1) / CH);
   if (blocks > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
@@ -122,10 +149,10 @@ cudaError_t launch_write_rows(const Geom& g, void* k, void* vt, const void* k_sr
   auto* vs = static_cast<const uint16_t*>(v_src);
   if (g.d == 128)
     write_rows_kernel<128><<<(unsigned)blocks, THREADS, 0, st>>>(g, kk, vv, ks, vs, n_group, n_tok, mode,
-                                                             row0, head, sync, tail_len, status);
+                                                             row0, head, sync, tail_len, status, acc);
   else
     write_rows_kernel<64><<<(unsigned)blocks, THREADS, 0, st>>>(g, kk, vv, ks, vs, n_group, n_tok, mode,
-                                                            row0, head, sync, tail_len, status);
+                                                            row0, head, sync, tail_len, status, acc);
   return cudaGetLastError();
 }
 
@@ -150,28 +177,6 @@ cudaError_t launch_rope_table(float* tab, int n_pos, int d, double theta, cudaSt
   const int blocks = (int)((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096);
   rope_table_kernel<<<blocks > 0 ? blocks : 1, 256, 0, st>>>(reinterpret_cast<float2*>(tab), n_pos,
                                                              d / 2, d, theta);
-  return cudaGetLastError();
-}
-
-// ---------------------------------------------------------------------------
-// Greedy longest-prefix acceptance, one thread per cache.
-
-__global__ void accept_kernel(int C, int blk, const int32_t* __restrict__ target,
-                              const int32_t* __restrict__ draft, int32_t* __restrict__ accept_len,
-                              int32_t* __restrict__ next_token) {
-  const int c = blockIdx.x * blockDim.x + threadIdx.x;
-  if (c >= C) return;
-  const int32_t* t = target + (size_t)c * blk;
-  const int32_t* dr = draft + (size_t)c * blk;
-  int k = 0;
-  while (k + 1 < blk && dr[k + 1] == t[k]) ++k;
-  accept_len[c] = k;
-  next_token[c] = t[k];
-}
-
-cudaError_t launch_accept(int C, int blk, const int32_t* target, const int32_t* draft,
-                          int32_t* accept_len, int32_t* next_token, cudaStream_t st) {
-  accept_kernel<<<(C + 127) / 128, 128, 0, st>>>(C, blk, target, draft, accept_len, next_token);
   return cudaGetLastError();
 }
 

@@ -8,15 +8,16 @@
 
 namespace skv {
 
+// mode 0: rows at row0; 1: frame insert (ring slot, head advance); 2: verify
+// block into the tail, with the accept length when target/draft are given.
 cudaError_t launch_write_rows(const Geom& g, void* k, void* vt, const void* k_src,
                               const void* v_src, int n_group, int n_tok, int mode, int row0,
                               int32_t* head, int32_t* sync, const int32_t* tail_len,
-                              int32_t* status, cudaStream_t st);
+                              int32_t* status, cudaStream_t st, const int32_t* target = nullptr,
+                              const int32_t* draft = nullptr, int32_t* accept_len = nullptr,
+                              int32_t* next_token = nullptr);
 
 cudaError_t launch_rope_table(float* tab, int n_pos, int d, double theta, cudaStream_t st);
-
-cudaError_t launch_accept(int C, int blk, const int32_t* target, const int32_t* draft,
-                          int32_t* accept_len, int32_t* next_token, cudaStream_t st);
 
 cudaError_t launch_attn_simple(const Geom& g, int Hq, int mode, int n_tok, const void* q,
                                void* out, float* lse, const int32_t* tail_len, const void* k,

@@ -101,8 +101,8 @@ enum {
   V_COUNT = V_DRAIN + 1
 };
 static_assert(VLayout<128>::NBAR >= V_COUNT, "barrier slots");
-// the merge keeps MAX_ROWS block rows x MAX_SPLITS weights in the K and V stages
-static_assert(KST * VLayout<64>::KT + VST * VLayout<64>::VT >= MAX_ROWS * MAX_SPLITS * 4, "merge scratch");
+// the merge keeps (m, l) of MAX_ROWS block rows x MAX_SPLITS pieces in the K and V stages
+static_assert(KST * VLayout<64>::KT + VST * VLayout<64>::VT >= 2 * MAX_ROWS * MAX_SPLITS * 4, "merge scratch");
 static_assert(MAX_ROWS <= QROWS, "block rows fit the query buffer");
 
 // One piece of a CTA's share: tiles [ta, ta + nt) of unit u, piece k of the
@@ -131,46 +131,91 @@ __host__ __device__ __forceinline__ int last_cta(long long u, int TM, int W) { r
 
 // O = sum_k 2^(m_k - M) O_k / sum_k 2^(m_k - M) l_k over the n pieces of
 // unit u, bf16 into the block rows; all threads of the CTA, with wts
-// (shared memory, R x n floats) for the per-row piece weights.
+// (shared memory, 2 x R x n floats) for the pieces' (m, l), then the per-row
+// weights.  The partials are read from L2 with many loads in flight: this
+// runs once the CTA's keys are done, on the kernel's tail.
 template <int D>
 __device__ __noinline__ void merge_pieces(const VerifyParams& p, int u, int n, int tid, float* wts) {
   const size_t base = (size_t)u * p.P_max;
   const int c = u / p.g.Hkv, h = u % p.g.Hkv;
-  for (int row = tid; row < p.R; row += NTHREADS) {
-    float M = -INFINITY;
-#pragma unroll 4
-    for (int k = 0; k < n; ++k) M = fmaxf(M, __ldcg(p.ws_ml + ((base + k) * p.R + row) * 2));
-    float den = 0.f;
-#pragma unroll 4
-    for (int k = 0; k < n; ++k) {
-      const float m = __ldcg(p.ws_ml + ((base + k) * p.R + row) * 2);
-      const float w = m == -INFINITY ? 0.f : exp2f(m - M);
-      wts[row * n + k] = w;
-      den += w * __ldcg(p.ws_ml + ((base + k) * p.R + row) * 2 + 1);
+  const int R = p.R;
+  float* wm = wts;           // [n][R]: m, then the weight
+  float* wl = wts + n * R;   // [n][R]: l
+  // every (piece, row) (m, l), four pairs per thread in flight
+  for (int i0 = tid; i0 < n * R; i0 += 4 * NTHREADS) {
+    float2 ml[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int i = i0 + q * NTHREADS;
+      ml[q] = i < n * R ? __ldcg(reinterpret_cast<const float2*>(p.ws_ml) + base * R + i) : make_float2(0.f, 0.f);
     }
-    const float inv = 1.f / den;
-    for (int k = 0; k < n; ++k) wts[row * n + k] *= inv;
-  }
-  __syncthreads();
-  for (int e = tid; e < p.R * (D / 4); e += NTHREADS) {
-    const int row = e / (D / 4), d4 = e % (D / 4);
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-    for (int k = 0; k < n; ++k) {
-      const float w = wts[row * n + k];
-      const float4 o = __ldcg(reinterpret_cast<const float4*>(p.ws_o + ((base + k) * p.R + row) * D) + d4);
-      if (w != 0.f) {
-        acc.x += w * o.x;
-        acc.y += w * o.y;
-        acc.z += w * o.z;
-        acc.w += w * o.w;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int i = i0 + q * NTHREADS;
+      if (i < n * R) {
+        wm[i] = ml[q].x;
+        wl[i] = ml[q].y;
       }
     }
-    const int jt = row / p.G, gq = row % p.G;
-    uint2 pk;
-    pk.x = pack_bf16x2(acc.x, acc.y);
-    pk.y = pack_bf16x2(acc.z, acc.w);
-    *reinterpret_cast<uint2*>(p.out + (((size_t)c * p.blk + jt) * p.Hq + h * p.G + gq) * D + d4 * 4) = pk;
+  }
+  __syncthreads();
+  for (int row = tid; row < R; row += NTHREADS) {
+    float M = -INFINITY;
+    for (int k = 0; k < n; ++k) M = fmaxf(M, wm[k * R + row]);
+    float den = 0.f;
+    for (int k = 0; k < n; ++k) {
+      const float m = wm[k * R + row];
+      const float w = m == -INFINITY ? 0.f : exp2f(m - M);
+      wm[k * R + row] = w;
+      den += w * wl[k * R + row];
+    }
+    const float inv = 1.f / den;
+    for (int k = 0; k < n; ++k) wm[k * R + row] *= inv;
+  }
+  __syncthreads();
+  // (row, 4 columns) items, two of them per thread and four pieces at a time in flight
+  constexpr int D4 = D / 4;
+  constexpr int IT = 2;
+  const int n_items = R * D4;
+  for (int e0 = tid; e0 < n_items; e0 += IT * NTHREADS) {
+    float4 acc[IT];
+#pragma unroll
+    for (int q = 0; q < IT; ++q) acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int k0 = 0; k0 < n; k0 += 4) {
+      float4 t[IT][4];
+      float w[IT][4];
+#pragma unroll
+      for (int q = 0; q < IT; ++q) {
+        const int e = e0 + q * NTHREADS, row = e < n_items ? e / D4 : 0, d4 = e % D4;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const int k = k0 + kk;
+          w[q][kk] = (e < n_items && k < n) ? wm[k * R + row] : 0.f;
+          t[q][kk] = w[q][kk] != 0.f ? __ldcg(reinterpret_cast<const float4*>(p.ws_o + ((base + k) * R + row) * D) + d4)
+                                     : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < IT; ++q)
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          acc[q].x += w[q][kk] * t[q][kk].x;
+          acc[q].y += w[q][kk] * t[q][kk].y;
+          acc[q].z += w[q][kk] * t[q][kk].z;
+          acc[q].w += w[q][kk] * t[q][kk].w;
+        }
+    }
+#pragma unroll
+    for (int q = 0; q < IT; ++q) {
+      const int e = e0 + q * NTHREADS;
+      if (e >= n_items) continue;
+      const int row = e / D4, d4 = e % D4;
+      const int jt = row / p.G, gq = row % p.G;
+      uint2 pk;
+      pk.x = pack_bf16x2(acc[q].x, acc[q].y);
+      pk.y = pack_bf16x2(acc[q].z, acc[q].w);
+      *reinterpret_cast<uint2*>(p.out + (((size_t)c * p.blk + jt) * p.Hq + h * p.G + gq) * D + d4 * 4) = pk;
+    }
   }
   __syncthreads();
 }
@@ -268,11 +313,16 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
     if (lane == 0) {
       tc::prefetch_tmap(is_k ? &tmap_k : &tmap_v);
       int gt = 0;
-      bool ok = true;
+      bool ok = true, tail_ready = false;
       for (int pi = 0; ok && pi < n_pieces; ++pi) {
         const int nt = P(pi, PC_NT), ta = P(pi, PC_TA), zc = P(pi, PC_U);
         for (int j = 0; j < nt; ++j) {
           const int s = gt % nst, u = gt / nst, r0 = (ta + j) * BN;
+          if (!tail_ready && r0 + BN > g.n_visual()) {
+            // rows of the tail: the block's K/V are written by the kernel before this one
+            asm volatile("griddepcontrol.wait;" ::: "memory");
+            tail_ready = true;
+          }
           if (gt >= nst && !(ok = tc::mbar_wait(bar((is_k ? V_KEMPTY : V_VEMPTY) + s), (u - 1) & 1, wait_ns, s_abort)))
             break;
           if (is_k) {
@@ -679,16 +729,26 @@ struct VerifyPlan {
   int TM, W, n_cta, P_max;
 };
 
-// Partition.  Two CTAs are resident per SM; the units' tiles are spread over
-// at most one wave of them, each CTA taking at least MIN_SHARE tiles and at
-// most MAX_PIECES - 2 whole units' worth (so its share has at most
-// MAX_PIECES pieces), every unit in at most MAX_SPLITS pieces, no CTA empty.
+// Partition.  Two CTAs are resident per SM.  When the units alone fill more
+// than half of that wave, each CTA takes one whole unit; otherwise the
+// units' tiles are spread over at most one wave, each CTA taking at least
+// MIN_SHARE tiles and at most MAX_PIECES - 2 whole units' worth (so its
+// share has at most MAX_PIECES pieces), every unit in at most MAX_SPLITS
+// pieces, no CTA empty.
 VerifyPlan verify_plan(const Geom& g) {
   VerifyPlan pl;
   const long long units = (long long)g.C * g.Hkv;
   pl.TM = (g.n_visual() + g.tail_cap + BN - 1) / BN;
   const long long total = units * pl.TM;
-  long long n = min(2LL * num_sms(), (total + MIN_SHARE - 1) / MIN_SHARE);
+  const long long slots = 2LL * num_sms();
+  if (units <= slots && 2 * units > slots) {
+    // one whole unit per CTA already fills most of the wave: no partials
+    pl.W = pl.TM;
+    pl.n_cta = (int)units;
+    pl.P_max = 1;
+    return pl;
+  }
+  long long n = min(slots, (total + MIN_SHARE - 1) / MIN_SHARE);
   n = max(n, (units + MAX_PIECES - 3) / (MAX_PIECES - 2));
   n = min(n, total / max(1LL, (long long)((pl.TM + MAX_SPLITS - 2) / (MAX_SPLITS - 1))));
   n = max(n, 1LL);
@@ -772,16 +832,28 @@ cudaError_t launch_verify_tc(const Geom& g, int Hq, int blk, const int32_t* tail
   p.status = status;
   p.scale_log2 = sm_scale * 1.4426950408889634f;
   p.wait_ns = wait_ns ? wait_ns : 2000000000ull;
+  // launched as a programmatic dependent of the tail write before it: set-up,
+  // query blocks and visual key tiles overlap that kernel, whose writes the
+  // producers wait for before they load a tile that reaches the tail
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = dim3((unsigned)pl.n_cta);
+  cfg.blockDim = dim3(NTHREADS);
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   if (g.d == 128) {
-    const int smem = VLayout<128>::ALLOC;
-    if ((e = set_smem_once(verify_tc_kernel<128>, smem, 0)) != cudaSuccess) return e;
-    verify_tc_kernel<128><<<(unsigned)pl.n_cta, NTHREADS, smem, st>>>(tk, tv, tq, p);
+    cfg.dynamicSmemBytes = VLayout<128>::ALLOC;
+    if ((e = set_smem_once(verify_tc_kernel<128>, VLayout<128>::ALLOC, 0)) != cudaSuccess) return e;
+    e = cudaLaunchKernelEx(&cfg, verify_tc_kernel<128>, tk, tv, tq, p);
   } else {
-    const int smem = VLayout<64>::ALLOC;
-    if ((e = set_smem_once(verify_tc_kernel<64>, smem, 1)) != cudaSuccess) return e;
-    verify_tc_kernel<64><<<(unsigned)pl.n_cta, NTHREADS, smem, st>>>(tk, tv, tq, p);
+    cfg.dynamicSmemBytes = VLayout<64>::ALLOC;
+    if ((e = set_smem_once(verify_tc_kernel<64>, VLayout<64>::ALLOC, 1)) != cudaSuccess) return e;
+    e = cudaLaunchKernelEx(&cfg, verify_tc_kernel<64>, tk, tv, tq, p);
   }
-  return cudaGetLastError();
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace skv

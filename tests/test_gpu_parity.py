@@ -145,6 +145,30 @@ def test_verify_alpamayo_batches(B):
     assert pair.cache.device_status() == 0
 
 
+def test_verify_full_block_rows_uneven_tails():
+    """64 block rows per kv head (blk 16, 4 query heads per kv head) and a
+    different tail length per cache: units end at different key tiles, so
+    some shares hold pieces past a unit's keys, and units span several
+    shares whose partials are merged."""
+    w = W["alpamayo_verify"].with_(C=6, blk=16)
+    tails = [0, 5, 16, 33, 60, 100]
+    pair = Pair(w, "vr")
+    pair.fill()
+    pair.insert()
+    tk, tv = synth.tail_kv(w, max(tails), pair.tag)
+    skv.kv_write_rows(pair.cache, pair.cache.n_visual, to_dev(tk), to_dev(tv))
+    for c in range(w.C):
+        pair.win[c].set_tail(tk[c][:tails[c]], tv[c][:tails[c]])
+    q, k, v = synth.verify_block(w, pair.tag)
+    tail = torch.tensor(tails, dtype=torch.int32, device="cuda")
+    out, _, _ = skv.stream_attn_verify(pair.cache, tail, to_dev(q), to_dev(k), to_dev(v), w.sm_scale)
+    got = bf16_dev_to_f64(out)
+    for c in range(w.C):
+        want, _ = O.stream_verify(pair.win[c], q[c], k[c], v[c], w.theta, w.sm_scale)
+        assert_close(got[c], want, "verify blk 16 cache %d (tail %d)" % (c, tails[c]))
+    assert pair.cache.device_status() == 0
+
+
 def test_verify_tiny_and_tail_advance():
     """Two verify rounds; the caller advances tail_len by accept_len + 1."""
     w = W["tiny"].with_(C=3, blk=9)
