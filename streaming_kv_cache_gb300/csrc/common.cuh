@@ -11,9 +11,26 @@
 
 namespace skv {
 
+// n / d and n % d by multiply-high for n < 2^31, d >= 1, with m =
+// floor((2^32 - 1) / d): the first quotient is floor(n/d) or one less
+// (n m / 2^32 undershoots n / d by less than 2n / 2^32 < 1), so a single
+// correction step makes it exact.
+__host__ __device__ __forceinline__ uint32_t fastdiv_m(uint32_t d) { return 0xFFFFFFFFu / d; }
+__device__ __forceinline__ int fastdiv(int n, int d, uint32_t m, int& rem) {
+  uint32_t q = __umulhi((uint32_t)n, m);
+  uint32_t r = (uint32_t)n - q * (uint32_t)d;
+  if (r >= (uint32_t)d) {
+    ++q;
+    r -= (uint32_t)d;
+  }
+  rem = (int)r;
+  return (int)q;
+}
+
 // Plain-value copy of the cache geometry that kernels receive by value.
 struct Geom {
   int C, V, F, T, P, tail_cap, Hkv, d, row_cap, rope_len;
+  uint32_t ft_m, t_m;   // fastdiv multipliers of F*T and T
   __host__ __device__ int ring_rows() const { return V * F * T; }
   __host__ __device__ int n_visual() const { return P + V * F * T; }
 };
@@ -23,24 +40,9 @@ inline Geom geom_of(const skv_cache& c) {
   g.C = c.n_cache; g.V = c.n_view; g.F = c.n_frame; g.T = c.frame_len; g.P = c.prefix_len;
   g.tail_cap = c.tail_cap; g.Hkv = c.n_kv_head; g.d = c.head_dim; g.row_cap = c.row_cap;
   g.rope_len = c.rope_len;
+  g.ft_m = fastdiv_m((uint32_t)(g.F * g.T > 0 ? g.F * g.T : 1));
+  g.t_m = fastdiv_m((uint32_t)(g.T > 0 ? g.T : 1));
   return g;
-}
-
-// Logical index (= rotary position) of physical key row r of cache c, given
-// that cache's ring heads.  The prefix and the tail sit at their own row;
-// ring row P + (v*F + s)*T + t holds logical frame f = (s - head[v]) mod F
-// of view v, at index P + v*F*T + f*T + t.
-__device__ __forceinline__ int key_index(const Geom& g, const int* __restrict__ head_c, int r) {
-  const int u = r - g.P;
-  if (u < 0 || u >= g.ring_rows()) return r;
-  const int FT = g.F * g.T;
-  const int v = u / FT;
-  const int rem = u - v * FT;
-  const int s = rem / g.T;
-  const int t = rem - s * g.T;
-  int f = s - head_c[v];
-  if (f < 0) f += g.F;
-  return g.P + v * FT + f * g.T + t;
 }
 
 // Logical index of token t of view v's newest frame (the new-frame queries).

@@ -19,11 +19,6 @@ cudaError_t launch_write_rows(const Geom& g, void* k, void* vt, const void* k_sr
 
 cudaError_t launch_rope_table(float* tab, int n_pos, int d, double theta, cudaStream_t st);
 
-cudaError_t launch_attn_simple(const Geom& g, int Hq, int mode, int n_tok, const void* q,
-                               void* out, float* lse, const int32_t* tail_len, const void* k,
-                               const void* vt, const float* rope, const int32_t* head,
-                               float sm_scale, int32_t* status, cudaStream_t st);
-
 cudaError_t launch_prefill_tc(const Geom& g, int Hq, const void* q, void* out, float* lse, const void* k,
                               const void* vt, const float* rope, const int32_t* head, float sm_scale,
                               int32_t* status, uint64_t wait_ns, cudaStream_t st);

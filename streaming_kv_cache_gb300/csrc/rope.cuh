@@ -48,10 +48,9 @@ __device__ __forceinline__ void key_pos_run(const Geom& g, const int* __restrict
     return;
   }
   const int FT = g.F * g.T;
-  const int v = u / FT;
-  const int rem = u - v * FT;
-  const int sl = rem / g.T;
-  const int t = rem - sl * g.T;
+  int rem, t;
+  const int v = fastdiv(u, FT, g.ft_m, rem);
+  const int sl = fastdiv(rem, g.T, g.t_m, t);
   int f = sl - heads[v];
   if (f < 0) f += g.F;
   pos = g.P + v * FT + f * g.T + t;
