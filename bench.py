@@ -92,9 +92,18 @@ def traffic_for(kernel_file: str):
     ent = d.get(kernel_file)
     if not ent:
         return None
-    src = os.path.join(ROOT, "streaming_kv_cache_gb300", "csrc", kernel_file)
-    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-    return ent["bytes_per_launch"] if ent.get("source_sha") == h else None
+    return ent["bytes_per_launch"] if ent.get("source_sha") == source_sha(kernel_file) else None
+
+
+def source_sha(kernel_file: str) -> str:
+    """Hash of a kernel's source file and every header of the library (the
+    kernels include them): a change to any of them voids recorded counters."""
+    csrc = os.path.join(ROOT, "streaming_kv_cache_gb300", "csrc")
+    h = hashlib.sha256(open(os.path.join(csrc, kernel_file), "rb").read())
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cuh", ".h")):
+            h.update(open(os.path.join(csrc, name), "rb").read())
+    return h.hexdigest()[:16]
 
 
 # ---------------------------------------------------------------------------
@@ -371,7 +380,7 @@ def main():
     nxt = torch.empty((vw.C,), dtype=torch.int32, device=dev)
     torch.cuda.synchronize()
 
-    launches_per_step = 1 + 1 + 3      # insert; prefill; verify tail write + attention + accept
+    launches_per_step = 1 + 1 + 2      # insert; prefill; verify: tail write (+ accept) and attention
     ev = {n: [] for n in ("insert", "prefill", "verify")}
 
     def step(record):

@@ -79,7 +79,8 @@ struct VLayout {
   static constexpr int PIECE_OFF = MISC_OFF + 64;                 // MAX_PIECES x 8 ints
   static constexpr int MERGE_OFF = PIECE_OFF + MAX_PIECES * 32;   // units to merge
   static constexpr int HEAD_OFF = MERGE_OFF + MAX_PIECES * 4;     // 4 RoPE warps x MAX_VIEWS heads
-  static constexpr int BYTES = HEAD_OFF + 4 * MAX_VIEWS * 4;
+  static constexpr int R64_OFF = HEAD_OFF + 4 * MAX_VIEWS * 4;     // 4 RoPE warps x R(BN) of every chunk
+  static constexpr int BYTES = R64_OFF + 4 * (D / 16) * 64;
   static constexpr int ALLOC = BYTES + 1024;
 };
 
@@ -427,6 +428,12 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
 #pragma unroll
     for (int w4 = 0; w4 < 4; ++w4) step4[w4] = __ldg(rope4 + (HALF + ea) / 2 + w4);   // R(1)
     const Ang8 step = ang8_from(step4);
+    // R(BN) of every chunk in this warp's shared memory: a thread's first row
+    // of the next tile, BN rows on inside the same run, is this tile's first
+    // row turned by R(BN), no table load
+    float4* s_r64 = reinterpret_cast<float4*>(smem + L::R64_OFF) + wr * NCH * 4;
+    if (ln < NCH * 4) s_r64[ln] = __ldg(rope4 + ((size_t)BN * HALF + (ln / 4) * 8) / 2 + ln % 4);
+    __syncwarp();
     int gt = 0, a = 0;
     bool ok = true, q_in_flight = false;
     for (int pi = 0; ok && pi < n_pieces; ++pi) {
@@ -488,7 +495,21 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         if (pf_pos >= 0)
           rotate_key_rows<NPT>(smem + L::K_OFF + s * L::KT, off_a, off_b, ca, cb, row_base, (ta + j) * BN + row_base,
                                row_lim, pf_pos, pf_run, pf, step, g, s_head, rope4, ea, HALF);
-        if (j + 1 < nt) fetch(j + 1);
+        if (j + 1 < nt) {
+          if (pf_pos >= 0 && pf_run > BN && (ta + j + 1) * BN + row_base < row_lim) {
+            const float4* r = s_r64 + ch * 4;
+#pragma unroll
+            for (int w4 = 0; w4 < 4; ++w4) {
+              const float4 c = pf[w4], t = r[w4];
+              pf[w4] = make_float4(c.x * t.x - c.y * t.y, c.y * t.x + c.x * t.y,
+                                   c.z * t.z - c.w * t.w, c.w * t.z + c.z * t.w);
+            }
+            pf_pos += BN;
+            pf_run -= BN;
+          } else {
+            fetch(j + 1);
+          }
+        }
         tc::fence_proxy_async_smem();
         __syncwarp();
         if (ln == 0) tc::mbar_arrive(bar(V_KROT + s));
