@@ -114,7 +114,8 @@ struct PrefillParams {
   uint64_t wait_ns;
 };
 
-template <int D>
+// SW: compiled for a wait limit under the suspend hint (see tc::bounded_wait)
+template <int D, bool SW>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                   const __grid_constant__ CUtensorMap tmap_q, const PrefillParams p) {
@@ -227,7 +228,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
         for (int j = 0; j < nt; ++j) {
           const int s = j % NST, u = j / NST, r0 = s_tiles[j];
           if (j >= NST &&
-              !tc::mbar_wait_cluster(bar((is_k ? B_KEMPTY : B_VEMPTY) + s), (u - 1) & 1, wait_ns, s_abort))
+              !tc::mbar_wait_cluster<SW>(bar((is_k ? B_KEMPTY : B_VEMPTY) + s), (u - 1) & 1, wait_ns, s_abort))
             break;
           if (is_k) {
             tc::mbar_arrive_expect_tx(bar(B_KFULL + s), L::KST);
@@ -244,17 +245,16 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
           }
           issued = j + 1;
         }
-        if (*s_abort) {
-          set_status(p.status, SKV_DEV_TIMEOUT);
-          // let the copies this thread started land before the CTA exits
-          if (is_k) {
-            volatile int never = 0;
-            tc::mbar_wait(bar(B_QLOAD), 0, DRAIN_NS, &never);
-          }
-          for (int j = max(0, issued - NST); j < issued; ++j) {
-            volatile int never = 0;
-            tc::mbar_wait(bar((is_k ? B_KFULL : B_VFULL) + j % NST), (j / NST) & 1, DRAIN_NS, &never);
-          }
+        if (*s_abort) set_status(p.status, SKV_DEV_TIMEOUT);
+        // the copies this thread started land before the CTA exits, whether or
+        // not their consumers (which may have given up) waited for them
+        if (is_k) {
+          volatile int never = 0;
+          tc::mbar_wait<SW>(bar(B_QLOAD), 0, DRAIN_NS, &never);
+        }
+        for (int j = max(0, issued - NST); j < issued; ++j) {
+          volatile int never = 0;
+          tc::mbar_wait<SW>(bar((is_k ? B_KFULL : B_VFULL) + j % NST), (j / NST) & 1, DRAIN_NS, &never);
         }
       }
     } else if (warp == WARP_VFWD) {
@@ -264,7 +264,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
       if (lane == 0 && nt > 0) {
         for (int j = 0; j < nt; ++j) {
           const int s = j % NST, u = j / NST;
-          if (!tc::mbar_wait(bar(B_VFULL + s), u & 1, wait_ns, s_abort)) {
+          if (!tc::mbar_wait<SW>(bar(B_VFULL + s), u & 1, wait_ns, s_abort)) {
             set_status(p.status, SKV_DEV_TIMEOUT);
             break;
           }
@@ -304,8 +304,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
                             (acc || kk > 0) ? 1u : 0u);
           }
         };
-        bool ok = tc::mbar_wait_short(bar(B_QFULL), 0, wait_ns, s_abort);
-        if (ok) ok = tc::mbar_wait_short(bar(B_KROT), 0, wait_ns, s_abort);
+        bool ok = tc::mbar_wait_short<SW>(bar(B_QFULL), 0, wait_ns, s_abort);
+        if (ok) ok = tc::mbar_wait_short<SW>(bar(B_KROT), 0, wait_ns, s_abort);
         if (ok) {
           tc::tc_fence_after();
           issue_qk(0, 0);
@@ -317,17 +317,17 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
         for (int j = 0; ok && j < nt; ++j) {
           const int s = j % NST;
           const int s2 = (j + 1) % NST, u2 = (j + 1) / NST;
-          if (!(ok = tc::mbar_wait_short(bar(B_PFULL), j & 1, wait_ns, s_abort))) break;
+          if (!(ok = tc::mbar_wait_short<SW>(bar(B_PFULL), j & 1, wait_ns, s_abort))) break;
           tc::tc_fence_after();
           issue_pv(0, s, j > 0);
           tc::mma_commit_pair(bar(B_ODONE));
           if (j + 1 < nt) {
-            if (!(ok = tc::mbar_wait_short(bar(B_KROT + s2), u2 & 1, wait_ns, s_abort))) break;
+            if (!(ok = tc::mbar_wait_short<SW>(bar(B_KROT + s2), u2 & 1, wait_ns, s_abort))) break;
             tc::tc_fence_after();
             issue_qk(0, s2);
             tc::mma_commit_pair(bar(B_SFULL));
           }
-          if (!(ok = tc::mbar_wait_short(bar(B_PFULL + 1), j & 1, wait_ns, s_abort))) break;
+          if (!(ok = tc::mbar_wait_short<SW>(bar(B_PFULL + 1), j & 1, wait_ns, s_abort))) break;
           tc::tc_fence_after();
           issue_pv(1, s, j > 0);
           tc::mma_commit_pair(bar(B_ODONE + 1));
@@ -344,7 +344,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
       }
       if (lane == 0 && nt > 0) {
         volatile int never = 0;
-        tc::mbar_wait_cluster(bar(B_DRAIN), 0, DRAIN_NS, &never);
+        tc::mbar_wait_cluster<SW>(bar(B_DRAIN), 0, DRAIN_NS, &never);
       }
     }
   } else if (warp >= WARP_ROPE) {
@@ -388,7 +388,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
 #pragma unroll 1
     for (int j = 0; j < nt; ++j) {
       const int s = j % NST, u = j / NST;
-      if (!tc::mbar_wait(bar(B_KFULL + s), u & 1, wait_ns, s_abort)) {
+      if (!tc::mbar_wait<SW>(bar(B_KFULL + s), u & 1, wait_ns, s_abort)) {
         set_status(p.status, SKV_DEV_TIMEOUT);
         break;
       }
@@ -427,7 +427,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
       // t0 + qi*TQ + r/G, head r%G); rotate in place, at each token's
       // logical position, into fp16.  Thread tid takes chunk ch (8
       // frequencies) of NCH consecutive rows, four rows at a time.
-      ok = __all_sync(0xffffffffu, tc::mbar_wait(bar(B_QLOAD), 0, wait_ns, s_abort));
+      ok = __all_sync(0xffffffffu, tc::mbar_wait<SW>(bar(B_QLOAD), 0, wait_ns, s_abort));
       if (ok) {
         constexpr int HALF = D / 2, NCH = HALF / 8;
         const int ch = tid % NCH, rr0 = (tid / NCH) * NCH;
@@ -467,7 +467,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
 #pragma unroll 1
     for (int j = 0; ok && j < nt; ++j) {
       // tcgen05.ld/st below are warp-collective: every branch around them is warp-uniform
-      ok = __all_sync(0xffffffffu, tc::mbar_wait_cluster(bar(B_SFULL + i), j & 1, wait_ns, s_abort));
+      ok = __all_sync(0xffffffffu, tc::mbar_wait_cluster<SW>(bar(B_SFULL + i), j & 1, wait_ns, s_abort));
       if (!ok) break;
       tc::tc_fence_after();
       // the whole 128-score row in one TMEM round trip
@@ -549,7 +549,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
     }
     if (!ok) set_status(p.status, SKV_DEV_TIMEOUT);
     bool done = ok && nt > 0;
-    if (done) done = __all_sync(0xffffffffu, tc::mbar_wait_cluster(bar(B_ODONE + i), (nt - 1) & 1, wait_ns, s_abort));
+    if (done) done = __all_sync(0xffffffffu, tc::mbar_wait_cluster<SW>(bar(B_ODONE + i), (nt - 1) & 1, wait_ns, s_abort));
     if (done) {
       tc::tc_fence_after();
       const float inv_l = 1.f / l;
@@ -592,7 +592,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
 // Raise the kernel's dynamic shared-memory limit once per device.
 template <typename K>
 cudaError_t set_smem_once(K kernel, int bytes, int variant) {
-  static int done[64][2];
+  static int done[64][4];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -688,15 +688,20 @@ cudaError_t launch_prefill_tc(const Geom& g, int Hq, const void* q, void* out, f
   const long long blocks = 2LL * g.C * g.Hkv * g.V * p.pairs;
   if (blocks <= 0) return cudaSuccess;
   if (blocks > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
-  if (g.d == 128) {
-    const int smem = Layout<128>::ALLOC;
-    if ((e = set_smem_once(prefill_tc_kernel<128>, smem, 0)) != cudaSuccess) return e;
-    prefill_tc_kernel<128><<<(unsigned)blocks, NTHREADS, smem, st>>>(tk, tv, tq, p);
-  } else {
-    const int smem = Layout<64>::ALLOC;
-    if ((e = set_smem_once(prefill_tc_kernel<64>, smem, 1)) != cudaSuccess) return e;
-    prefill_tc_kernel<64><<<(unsigned)blocks, NTHREADS, smem, st>>>(tk, tv, tq, p);
-  }
+  const bool sw = p.wait_ns < tc::kSuspendHintNs;
+  auto launch = [&](auto kernel, int smem, int variant) -> cudaError_t {
+    cudaError_t err = set_smem_once(kernel, smem, variant);
+    if (err != cudaSuccess) return err;
+    kernel<<<(unsigned)blocks, NTHREADS, smem, st>>>(tk, tv, tq, p);
+    return cudaSuccess;
+  };
+  if (g.d == 128)
+    e = sw ? launch(prefill_tc_kernel<128, true>, Layout<128>::ALLOC, 2)
+           : launch(prefill_tc_kernel<128, false>, Layout<128>::ALLOC, 0);
+  else
+    e = sw ? launch(prefill_tc_kernel<64, true>, Layout<64>::ALLOC, 3)
+           : launch(prefill_tc_kernel<64, false>, Layout<64>::ALLOC, 1);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -70,35 +70,54 @@ __device__ __forceinline__ bool mbar_try_wait_short(uint32_t bar, uint32_t parit
 // Poll try(bar, parity) until it succeeds.  The wait is bounded: after
 // limit_ns nanoseconds (counted in SM cycles at the 2.07 GHz maximum clock,
 // so a slower clock only lengthens it) it raises *abort and returns false; it
-// also returns false once another thread has raised *abort.
-template <typename Try>
+// also returns false once another thread has raised *abort.  A suspended
+// try_wait may sleep up to the suspend hint, and the clock is read every 64
+// polls, so a limit far under the hint is not kept; kernels compiled with
+// SHORT (chosen by the host for such limits) poll without suspending and read
+// the clock at every poll instead.
+template <bool SHORT, typename Try>
 __device__ __forceinline__ bool bounded_wait(Try try_fn, uint32_t bar, uint32_t parity, uint64_t limit_ns,
                                              volatile int* abort) {
-  if (try_fn(bar, parity)) return true;
-  const long long limit = (long long)(limit_ns * 2.07);
-  const long long t0 = clock64();
-  for (uint32_t it = 1;; ++it) {
-    if (try_fn(bar, parity)) return true;
-    if ((it & 63) == 0) {
-      if (*abort) return false;
+  if constexpr (SHORT) {
+    const long long limit = (long long)(limit_ns * 2.07);
+    const long long t0 = clock64();
+    for (;;) {
+      if (mbar_try_wait_short(bar, parity)) return true;
       if (clock64() - t0 > limit) {
         *abort = 1;
         return false;
+      }
+      if (*abort) return false;
+    }
+  } else {
+    if (try_fn(bar, parity)) return true;
+    const long long limit = (long long)(limit_ns * 2.07);
+    const long long t0 = clock64();
+    for (uint32_t it = 1;; ++it) {
+      if (try_fn(bar, parity)) return true;
+      if ((it & 63) == 0) {
+        if (*abort) return false;
+        if (clock64() - t0 > limit) {
+          *abort = 1;
+          return false;
+        }
       }
     }
   }
 }
 
 // Wait for the phase with the given parity to complete (bounded, see bounded_wait).
+template <bool SHORT = false>
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns,
                                           volatile int* abort) {
-  return bounded_wait(mbar_try_wait, bar, parity, limit_ns, abort);
+  return bounded_wait<SHORT>(mbar_try_wait, bar, parity, limit_ns, abort);
 }
 
 // The same with short polls, for the MMA issuer.
+template <bool SHORT = false>
 __device__ __forceinline__ bool mbar_wait_short(uint32_t bar, uint32_t parity, uint64_t limit_ns,
                                                 volatile int* abort) {
-  return bounded_wait(mbar_try_wait_short, bar, parity, limit_ns, abort);
+  return bounded_wait<SHORT>(mbar_try_wait_short, bar, parity, limit_ns, abort);
 }
 
 // A value the compiler must (re)compute where it stands: keeps loop-invariant
@@ -178,9 +197,10 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
 
 // Bounded wait (as mbar_wait) with cluster-scope acquire: for barriers that
 // receive arrivals from the peer CTA or from a pair MMA's commit.
+template <bool SHORT = false>
 __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, uint64_t limit_ns,
                                                   volatile int* abort) {
-  return bounded_wait(mbar_try_wait_cluster, bar, parity, limit_ns, abort);
+  return bounded_wait<SHORT>(mbar_try_wait_cluster, bar, parity, limit_ns, abort);
 }
 
 __device__ __forceinline__ void cluster_sync() {

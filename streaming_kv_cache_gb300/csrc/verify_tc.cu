@@ -221,7 +221,8 @@ __device__ __noinline__ void merge_pieces(const VerifyParams& p, int u, int n, i
   __syncthreads();
 }
 
-template <int D>
+// SW: compiled for a wait limit under the suspend hint (see tc::bounded_wait)
+template <int D, bool SW>
 __global__ void __launch_bounds__(NTHREADS, 2)
 verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                  const __grid_constant__ CUtensorMap tmap_q, const VerifyParams p) {
@@ -324,7 +325,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
             asm volatile("griddepcontrol.wait;" ::: "memory");
             tail_ready = true;
           }
-          if (gt >= nst && !(ok = tc::mbar_wait(bar((is_k ? V_KEMPTY : V_VEMPTY) + s), (u - 1) & 1, wait_ns, s_abort)))
+          if (gt >= nst && !(ok = tc::mbar_wait<SW>(bar((is_k ? V_KEMPTY : V_VEMPTY) + s), (u - 1) & 1, wait_ns, s_abort)))
             break;
           if (is_k) {
             tc::mbar_arrive_expect_tx(bar(V_KFULL + s), L::KT);
@@ -338,13 +339,12 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
           ++gt;
         }
       }
-      if (!ok) {
-        set_status(p.status, SKV_DEV_TIMEOUT);
-        // let the copies this thread started land before the CTA exits
-        for (int j = max(0, gt - nst); j < gt; ++j) {
-          volatile int never = 0;
-          tc::mbar_wait(bar((is_k ? V_KFULL : V_VFULL) + j % nst), (j / nst) & 1, DRAIN_NS, &never);
-        }
+      if (!ok) set_status(p.status, SKV_DEV_TIMEOUT);
+      // the copies this thread started land before the CTA exits, whether or
+      // not their consumers (which may have given up) waited for them
+      for (int j = max(0, gt - nst); j < gt; ++j) {
+        volatile int never = 0;
+        tc::mbar_wait<SW>(bar((is_k ? V_KFULL : V_VFULL) + j % nst), (j / nst) & 1, DRAIN_NS, &never);
       }
     }
   } else if (warp == WARP_MMA) {
@@ -371,10 +371,10 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
       // PV of the CTA's tile gg; `first` = the piece's first, which starts O afresh
       auto issue_pv = [&](int gg, bool first) {
         const int vs = gg % VST, vu = gg / VST;
-        if (!(ok = tc::mbar_wait_short(bar(V_VFULL + vs), vu & 1, wait_ns, s_abort))) return;
-        if (!(ok = tc::mbar_wait_short(bar(V_PFULL + (gg & 1)), (gg >> 1) & 1, wait_ns, s_abort))) return;
+        if (!(ok = tc::mbar_wait_short<SW>(bar(V_VFULL + vs), vu & 1, wait_ns, s_abort))) return;
+        if (!(ok = tc::mbar_wait_short<SW>(bar(V_PFULL + (gg & 1)), (gg >> 1) & 1, wait_ns, s_abort))) return;
         // the softmax warps have read the previous piece's O out
-        if (first && a > 0 && !(ok = tc::mbar_wait_short(bar(V_OFREE), (a - 1) & 1, wait_ns, s_abort))) return;
+        if (first && a > 0 && !(ok = tc::mbar_wait_short<SW>(bar(V_OFREE), (a - 1) & 1, wait_ns, s_abort))) return;
         tc::tc_fence_after();
         const uint64_t dv = tc::opaque(dv0 + ((uint32_t)(vs * L::VT) >> 4));
         const uint32_t a_tmem = tmem + (gg & 1) * BN;
@@ -388,10 +388,10 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
       for (int pi = 0; ok && pi < n_pieces; ++pi) {
         const int nt = P(pi, PC_NT);
         if (nt == 0) continue;
-        if (!(ok = tc::mbar_wait_short(bar(V_QFULL), a & 1, wait_ns, s_abort))) break;
+        if (!(ok = tc::mbar_wait_short<SW>(bar(V_QFULL), a & 1, wait_ns, s_abort))) break;
         for (int j = 0; ok && j < nt; ++j) {
           const int gg = gt + j;
-          if (!(ok = tc::mbar_wait_short(bar(V_KROT + gg % KST), (gg / KST) & 1, wait_ns, s_abort))) break;
+          if (!(ok = tc::mbar_wait_short<SW>(bar(V_KROT + gg % KST), (gg / KST) & 1, wait_ns, s_abort))) break;
           tc::tc_fence_after();
           issue_qk(gg);
           tc::mma_commit(bar(V_SFULL + (gg & 1)));
@@ -408,7 +408,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
       // every MMA issued completes before TMEM is released
       tc::mma_commit(bar(V_DRAIN));
       volatile int never = 0;
-      tc::mbar_wait(bar(V_DRAIN), 0, DRAIN_NS, &never);
+      tc::mbar_wait<SW>(bar(V_DRAIN), 0, DRAIN_NS, &never);
     }
   } else if (warp >= WARP_ROPE) {
     // ----------------------------------------------------------------- RoPE
@@ -446,7 +446,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
       __syncwarp();
       // the query block of this piece: rows n = (token n / G, head n % G),
       // by TMA once the previous piece's QK MMAs are done with the buffer
-      if (a > 0 && !(ok = tc::mbar_wait(bar(V_QEMPTY), (a - 1) & 1, wait_ns, s_abort))) break;
+      if (a > 0 && !(ok = tc::mbar_wait<SW>(bar(V_QEMPTY), (a - 1) & 1, wait_ns, s_abort))) break;
       if (rt == 0) {
         tc::mbar_arrive_expect_tx(bar(V_QLOAD), p.R * 128 * (D / 64));
 #pragma unroll
@@ -454,7 +454,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
           tc::tma_load_3d(sbase + L::Q_OFF + hf * L::HALF_Q, &tmap_q, bar(V_QLOAD), hf * 64, h * p.G, c * p.blk);
         q_in_flight = true;
       }
-      if (!(ok = tc::mbar_wait(bar(V_QLOAD), a & 1, wait_ns, s_abort))) break;
+      if (!(ok = tc::mbar_wait<SW>(bar(V_QLOAD), a & 1, wait_ns, s_abort))) break;
       q_in_flight = false;
       // rotate the block rows in place at their tokens' positions (fp16 out)
       for (int it = rt; it < p.R * NCH; it += 128) {
@@ -491,7 +491,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
 #pragma unroll 1
       for (int j = 0; j < nt; ++j) {
         const int gg = gt + j, s = gg % KST;
-        if (!(ok = tc::mbar_wait(bar(V_KFULL + s), (gg / KST) & 1, wait_ns, s_abort))) break;
+        if (!(ok = tc::mbar_wait<SW>(bar(V_KFULL + s), (gg / KST) & 1, wait_ns, s_abort))) break;
         if (pf_pos >= 0)
           rotate_key_rows<NPT>(smem + L::K_OFF + s * L::KT, off_a, off_b, ca, cb, row_base, (ta + j) * BN + row_base,
                                row_lim, pf_pos, pf_run, pf, step, g, s_head, rope4, ea, HALF);
@@ -522,7 +522,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
       if (q_in_flight) {
         // let the query copy this thread started land before the CTA exits
         volatile int never = 0;
-        tc::mbar_wait(bar(V_QLOAD), a & 1, DRAIN_NS, &never);
+        tc::mbar_wait<SW>(bar(V_QLOAD), a & 1, DRAIN_NS, &never);
       }
     }
   } else {
@@ -549,7 +549,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
       for (int j = 0; j < nt; ++j) {
         const int gg = gt + j, sb = gg & 1;
         // tcgen05.ld/st below are warp-collective: every branch around them is warp-uniform
-        ok = __all_sync(0xffffffffu, tc::mbar_wait(bar(V_SFULL + sb), (gg >> 1) & 1, wait_ns, s_abort));
+        ok = __all_sync(0xffffffffu, tc::mbar_wait<SW>(bar(V_SFULL + sb), (gg >> 1) & 1, wait_ns, s_abort));
         if (!ok) break;
         tc::tc_fence_after();
         const uint32_t tS = tmem + t_lane + sb * BN;
@@ -578,7 +578,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
           m_used = (mx == -INFINITY) ? 0.f : mx;
         } else if (__any_sync(0xffffffffu, grow)) {
           // PV of the previous tile must have landed in O before it is rescaled
-          ok = __all_sync(0xffffffffu, tc::mbar_wait(bar(V_PVDONE), (gg - 1) & 1, wait_ns, s_abort));
+          ok = __all_sync(0xffffffffu, tc::mbar_wait<SW>(bar(V_PVDONE), (gg - 1) & 1, wait_ns, s_abort));
           if (!ok) break;
           tc::tc_fence_after();
           const float m_new = grow ? mx : m_used;
@@ -627,7 +627,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(bar(V_PFULL + sb));
       }
-      if (ok && nt > 0) ok = __all_sync(0xffffffffu, tc::mbar_wait(bar(V_ODONE), a & 1, wait_ns, s_abort));
+      if (ok && nt > 0) ok = __all_sync(0xffffffffu, tc::mbar_wait<SW>(bar(V_ODONE), a & 1, wait_ns, s_abort));
       // both softmax warps take the same path from here (named barriers below)
       if (lane == 0) s_info[2 + warp] = ok;
       asm volatile("bar.sync 1, %0;" ::"r"(SOFTMAX_THREADS) : "memory");
@@ -736,7 +736,7 @@ int num_sms() {
 // Raise the kernel's dynamic shared-memory limit once per device.
 template <typename K>
 cudaError_t set_smem_once(K kernel, int bytes, int variant) {
-  static int done[64][2];
+  static int done[64][4];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -865,15 +865,19 @@ cudaError_t launch_verify_tc(const Geom& g, int Hq, int blk, const int32_t* tail
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (g.d == 128) {
-    cfg.dynamicSmemBytes = VLayout<128>::ALLOC;
-    if ((e = set_smem_once(verify_tc_kernel<128>, VLayout<128>::ALLOC, 0)) != cudaSuccess) return e;
-    e = cudaLaunchKernelEx(&cfg, verify_tc_kernel<128>, tk, tv, tq, p);
-  } else {
-    cfg.dynamicSmemBytes = VLayout<64>::ALLOC;
-    if ((e = set_smem_once(verify_tc_kernel<64>, VLayout<64>::ALLOC, 1)) != cudaSuccess) return e;
-    e = cudaLaunchKernelEx(&cfg, verify_tc_kernel<64>, tk, tv, tq, p);
-  }
+  const bool sw = p.wait_ns < tc::kSuspendHintNs;
+  auto launch = [&](auto kernel, int smem, int variant) -> cudaError_t {
+    cudaError_t err = set_smem_once(kernel, smem, variant);
+    if (err != cudaSuccess) return err;
+    cfg.dynamicSmemBytes = smem;
+    return cudaLaunchKernelEx(&cfg, kernel, tk, tv, tq, p);
+  };
+  if (g.d == 128)
+    e = sw ? launch(verify_tc_kernel<128, true>, VLayout<128>::ALLOC, 2)
+           : launch(verify_tc_kernel<128, false>, VLayout<128>::ALLOC, 0);
+  else
+    e = sw ? launch(verify_tc_kernel<64, true>, VLayout<64>::ALLOC, 3)
+           : launch(verify_tc_kernel<64, false>, VLayout<64>::ALLOC, 1);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
