@@ -242,6 +242,8 @@ def run_only(args):
         return (torch.randn(shape, generator=gen, device=dev) * scale).to(torch.bfloat16)
 
     w = (VERIFY_W if args.only == "verify" else PREFILL_W).with_(C=args.layers)
+    if args.only == "verify" and args.blk:
+        w = w.with_(blk=args.blk)
     cache = skv.StreamCache(w.C, w.P, w.V, w.F, w.T, w.Hkv, w.d, w.theta, tail_cap=w.tail_cap)
     skv.kv_write_rows(cache, 0, randn((w.C, w.P, w.Hkv, w.d)), randn((w.C, w.P, w.Hkv, w.d)))
     k_new = randn((w.C, w.V, w.T, w.Hkv, w.d))
@@ -310,6 +312,8 @@ def main():
                     help="profiling aid: time one kernel alone on a reduced case and print its ms")
     ap.add_argument("--layers", type=int, default=4,
                     help="layer caches (prefill/insert) or batch (verify) of the --only case")
+    ap.add_argument("--blk", type=int, default=None,
+                    help="verify block size of the --only verify case (default: the workload's 9)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

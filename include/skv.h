@@ -229,7 +229,9 @@ size_t skv_verify_workspace_bytes(const skv_cache* cache, int32_t n_q_head, int3
  * ws: device workspace of ws_bytes >= skv_verify_workspace_bytes(); it must
  *     be zero-filled before its first use, the call leaves it ready for the
  *     next one (re-zero it after a call that set a device status bit).
- * Needs 1 <= blk, blk * (Hq/Hkv) <= 64 (block rows per kv head).  tail_len + blk > tail_cap sets
+ * Needs 1 <= blk <= tail_cap and Hq/Hkv <= 64; a block of more than 64 rows
+ * per kv head (blk * Hq/Hkv) is taken 64 rows at a time, which needs Hq/Hkv to
+ * divide 64.  tail_len + blk > tail_cap sets
  * SKV_DEV_TAIL_OVERFLOW and skips that cache.
  */
 int stream_attn_verify(const skv_cache* cache, int32_t n_q_head, int32_t blk,

@@ -171,7 +171,11 @@ int stream_attn_verify(const skv_cache* cache, int32_t n_q_head, int32_t blk,
   if (rc) return rc;
   if (n_q_head < 1 || n_q_head % cache->n_kv_head) return SKV_ERR_INVALID;
   if (blk < 1 || blk > cache->tail_cap) return SKV_ERR_INVALID;
-  if ((long long)blk * (n_q_head / cache->n_kv_head) > 64) return SKV_ERR_UNSUPPORTED;
+  {
+    // block rows are taken 64 at a time per kv head, whole tokens each
+    const int G = n_q_head / cache->n_kv_head;
+    if (G > 64 || ((long long)blk * G > 64 && 64 % G)) return SKV_ERR_UNSUPPORTED;
+  }
   if (!(sm_scale > 0.f) || sm_scale != sm_scale) return SKV_ERR_INVALID;
   if (cache->n_cache == 0) return SKV_OK;
   if (!tail_len || !q_blk || !k_blk || !v_blk || !out) return SKV_ERR_INVALID;

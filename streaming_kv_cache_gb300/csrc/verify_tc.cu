@@ -113,6 +113,7 @@ enum { PC_U = 0, PC_TA, PC_NT, PC_TL, PC_K, PC_N, PC_OK, PC_G0 };
 struct VerifyParams {
   Geom g;
   int Hq, G, blk, R;          // R = blk * G block rows per kv head
+  int RH, RU, TQH;            // row halves per kv head (64 block rows each), rows per unit at most, tokens per query box
   int TM, W, P_max;           // tiles per unit, tiles per CTA, pieces per unit at most
   int units;
   const int32_t* tail_len;
@@ -138,8 +139,11 @@ __host__ __device__ __forceinline__ int last_cta(long long u, int TM, int W) { r
 template <int D>
 __device__ __noinline__ void merge_pieces(const VerifyParams& p, int u, int n, int tid, float* wts) {
   const size_t base = (size_t)u * p.P_max;
-  const int c = u / p.g.Hkv, h = u % p.g.Hkv;
-  const int R = p.R;
+  const int plane = u / p.RH, rh = u % p.RH;
+  const int c = plane / p.g.Hkv, h = plane % p.g.Hkv;
+  const int row0 = rh * MAX_ROWS;                    // first block row of this unit
+  const int R = min(p.RU, p.R - row0);               // its rows
+  const int RS = p.RU;                               // row stride of the workspace
   float* wm = wts;           // [n][R]: m, then the weight
   float* wl = wts + n * R;   // [n][R]: l
   // every (piece, row) (m, l), four pairs per thread in flight
@@ -148,7 +152,8 @@ __device__ __noinline__ void merge_pieces(const VerifyParams& p, int u, int n, i
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       const int i = i0 + q * NTHREADS;
-      ml[q] = i < n * R ? __ldcg(reinterpret_cast<const float2*>(p.ws_ml) + base * R + i) : make_float2(0.f, 0.f);
+      ml[q] = i < n * R ? __ldcg(reinterpret_cast<const float2*>(p.ws_ml) + (base + i / R) * RS + i % R)
+                        : make_float2(0.f, 0.f);
     }
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
@@ -192,7 +197,7 @@ __device__ __noinline__ void merge_pieces(const VerifyParams& p, int u, int n, i
         for (int kk = 0; kk < 4; ++kk) {
           const int k = k0 + kk;
           w[q][kk] = (e < n_items && k < n) ? wm[k * R + row] : 0.f;
-          t[q][kk] = w[q][kk] != 0.f ? __ldcg(reinterpret_cast<const float4*>(p.ws_o + ((base + k) * R + row) * D) + d4)
+          t[q][kk] = w[q][kk] != 0.f ? __ldcg(reinterpret_cast<const float4*>(p.ws_o + ((base + k) * RS + row) * D) + d4)
                                      : make_float4(0.f, 0.f, 0.f, 0.f);
         }
       }
@@ -211,7 +216,7 @@ __device__ __noinline__ void merge_pieces(const VerifyParams& p, int u, int n, i
       const int e = e0 + q * NTHREADS;
       if (e >= n_items) continue;
       const int row = e / D4, d4 = e % D4;
-      const int jt = row / p.G, gq = row % p.G;
+      const int jt = (row0 + row) / p.G, gq = (row0 + row) % p.G;
       uint2 pk;
       pk.x = pack_bf16x2(acc[q].x, acc[q].y);
       pk.y = pack_bf16x2(acc[q].z, acc[q].w);
@@ -261,7 +266,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
       const int u = (int)(gg / p.TM);
       const int ta = (int)(gg - (long long)u * p.TM);
       const int tb = (int)min((long long)p.TM, g1 - (long long)u * p.TM);
-      const int c = u / g.Hkv;
+      const int c = u / p.RH / g.Hkv;
       // unit checks, one lane per view: ring heads in range, tail within its capacity
       const int tl = p.tail_len[c];
       bool head_ok = true;
@@ -317,7 +322,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
       int gt = 0;
       bool ok = true, tail_ready = false;
       for (int pi = 0; ok && pi < n_pieces; ++pi) {
-        const int nt = P(pi, PC_NT), ta = P(pi, PC_TA), zc = P(pi, PC_U);
+        const int nt = P(pi, PC_NT), ta = P(pi, PC_TA), zc = P(pi, PC_U) / p.RH;
         for (int j = 0; j < nt; ++j) {
           const int s = gt % nst, u = gt / nst, r0 = (ta + j) * BN;
           if (!tail_ready && r0 + BN > g.n_visual()) {
@@ -440,7 +445,8 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
       const int nt = P(pi, PC_NT);
       if (nt == 0) continue;
       const int u = P(pi, PC_U), ta = P(pi, PC_TA);
-      const int c = u / g.Hkv, h = u % g.Hkv;
+      const int plane = u / p.RH, c = plane / g.Hkv, h = plane % g.Hkv;
+      const int row0 = (u % p.RH) * MAX_ROWS, R_u = min(p.RU, p.R - row0);   // this unit's block rows
       const int q_base = g.n_visual() + P(pi, PC_TL);   // logical index of block token 0
       for (int v = ln; v < g.V; v += 32) s_head[v] = p.head[(size_t)c * g.V + v];
       __syncwarp();
@@ -448,23 +454,25 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
       // by TMA once the previous piece's QK MMAs are done with the buffer
       if (a > 0 && !(ok = tc::mbar_wait<SW>(bar(V_QEMPTY), (a - 1) & 1, wait_ns, s_abort))) break;
       if (rt == 0) {
-        tc::mbar_arrive_expect_tx(bar(V_QLOAD), p.R * 128 * (D / 64));
+        tc::mbar_arrive_expect_tx(bar(V_QLOAD), p.TQH * p.G * 128 * (D / 64));
 #pragma unroll
         for (int hf = 0; hf < D / 64; ++hf)
-          tc::tma_load_3d(sbase + L::Q_OFF + hf * L::HALF_Q, &tmap_q, bar(V_QLOAD), hf * 64, h * p.G, c * p.blk);
+          tc::tma_load_3d(sbase + L::Q_OFF + hf * L::HALF_Q, &tmap_q, bar(V_QLOAD), hf * 64, h * p.G,
+                          c * p.blk + row0 / p.G);
         q_in_flight = true;
       }
       if (!(ok = tc::mbar_wait<SW>(bar(V_QLOAD), a & 1, wait_ns, s_abort))) break;
       q_in_flight = false;
       // rotate the block rows in place at their tokens' positions (fp16 out)
-      for (int it = rt; it < p.R * NCH; it += 128) {
+      for (int it = rt; it < R_u * NCH; it += 128) {
         const int n = it / NCH, cq = it % NCH;
         const int qa = cq * 8, qb = HALF + cq * 8;
         uint4* pa = reinterpret_cast<uint4*>(smem + L::Q_OFF + (qa / 64) * L::HALF_Q + tc::sw128_off(n, (qa % 64) / 8));
         uint4* pb = reinterpret_cast<uint4*>(smem + L::Q_OFF + (qb / 64) * L::HALF_Q + tc::sw128_off(n, (qb % 64) / 8));
         float4 cs[4];
 #pragma unroll
-        for (int w4 = 0; w4 < 4; ++w4) cs[w4] = __ldg(rope4 + ((size_t)(q_base + n / p.G) * HALF + qa) / 2 + w4);
+        for (int w4 = 0; w4 < 4; ++w4)
+          cs[w4] = __ldg(rope4 + ((size_t)(q_base + (row0 + n) / p.G) * HALF + qa) / 2 + w4);
         uint4 xa = *pa, xb = *pb;
         rotate_pairs4(xa, xb, cs);
         *pa = xa;
@@ -527,19 +535,20 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
     }
   } else {
     // ------------------------------------------------- softmax + epilogue
-    const int row = warp * 32 + lane;            // TMEM lane = block row (warps 0, 1)
+    const int row = warp * 32 + lane;            // TMEM lane = the unit's block row (warps 0, 1)
     const uint32_t t_lane = (uint32_t)(warp * 32) << 16;
     const uint32_t tO = tmem + t_lane + 128;
-    const bool valid = row < p.R;
-    const int jt = valid ? row / p.G : 0;
-    const int gq = valid ? row % p.G : 0;
     const float sl = p.scale_log2;
     int gt = 0, a = 0;
     bool alive = true;
     for (int pi = 0; alive && pi < n_pieces; ++pi) {
       if (!P(pi, PC_OK)) continue;      // a skipped cache: no piece of its units arrives
       const int nt = P(pi, PC_NT), u = P(pi, PC_U), n_unit = P(pi, PC_N);
-      const int c = u / g.Hkv, h = u % g.Hkv;
+      const int plane = u / p.RH, c = plane / g.Hkv, h = plane % g.Hkv;
+      const int brow = (u % p.RH) * MAX_ROWS + row;   // block row of this lane
+      const bool valid = brow < p.R;
+      const int jt = valid ? brow / p.G : 0;
+      const int gq = valid ? brow % p.G : 0;
       const bool multi = n_unit > 1;
       const size_t slot = (size_t)u * p.P_max + P(pi, PC_K);
       const int lim = g.n_visual() + P(pi, PC_TL) + jt;   // largest key index this row may see
@@ -658,7 +667,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
             }
           }
         } else {
-          float* orow = p.ws_o + (slot * p.R + row) * D;
+          float* orow = p.ws_o + (slot * p.RU + row) * D;
 #pragma unroll 1
           for (int cb = 0; cb < D / 32; ++cb) {
             uint32_t o[32];
@@ -679,8 +688,8 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
       if (multi) {
         // this piece's share (empty when it lies past the unit's keys)
         if (valid) {
-          p.ws_ml[(slot * p.R + row) * 2] = nt > 0 ? m_used : -INFINITY;
-          p.ws_ml[(slot * p.R + row) * 2 + 1] = nt > 0 ? l : 0.f;
+          p.ws_ml[(slot * p.RU + row) * 2] = nt > 0 ? m_used : -INFINITY;
+          p.ws_ml[(slot * p.RU + row) * 2 + 1] = nt > 0 ? l : 0.f;
         }
         asm volatile("bar.sync 1, %0;" ::"r"(SOFTMAX_THREADS) : "memory");
         if (tid == 0) {
@@ -756,9 +765,9 @@ struct VerifyPlan {
 // MIN_SHARE tiles and at most MAX_PIECES - 2 whole units' worth (so its
 // share has at most MAX_PIECES pieces), every unit in at most MAX_SPLITS
 // pieces, no CTA empty.
-VerifyPlan verify_plan(const Geom& g) {
+VerifyPlan verify_plan(const Geom& g, int RH) {
   VerifyPlan pl;
-  const long long units = (long long)g.C * g.Hkv;
+  const long long units = (long long)g.C * g.Hkv * RH;
   pl.TM = (g.n_visual() + g.tail_cap + BN - 1) / BN;
   const long long total = units * pl.TM;
   const long long slots = 2LL * num_sms();
@@ -790,13 +799,19 @@ bool all_single(const VerifyPlan& pl, long long units) {
 
 }  // namespace
 
+// Block rows per kv head in units of at most MAX_ROWS: each (cache, kv head,
+// row half) is one work unit that streams the plane's keys.
+int row_halves(int Hq, int Hkv, int blk) { return (blk * (Hq / Hkv) + MAX_ROWS - 1) / MAX_ROWS; }
+
 // Workspace: [units] int32 counters (256-byte aligned block), then the fp32
-// partial O rows and the (m, l) pairs of units x P_max piece slots.
+// partial O rows and the (m, l) pairs of units x P_max piece slots, each slot
+// holding a unit's (at most MAX_ROWS) rows.
 size_t verify_ws_bytes(const Geom& g, int Hq, int blk) {
-  const VerifyPlan pl = verify_plan(g);
-  const size_t units = (size_t)g.C * g.Hkv;
+  const int RH = row_halves(Hq, g.Hkv, blk);
+  const VerifyPlan pl = verify_plan(g, RH);
+  const size_t units = (size_t)g.C * g.Hkv * RH;
   if (units == 0 || all_single(pl, (long long)units)) return 0;
-  const size_t rows = units * pl.P_max * blk * (Hq / g.Hkv);
+  const size_t rows = units * pl.P_max * min(blk * (Hq / g.Hkv), MAX_ROWS);
   return (units * 4 + 255) / 256 * 256 + rows * (g.d + 2) * sizeof(float);
 }
 
@@ -808,19 +823,22 @@ cudaError_t launch_verify_tc(const Geom& g, int Hq, int blk, const int32_t* tail
                              const void* k, const void* vt, const float* rope, const int32_t* head,
                              void* ws, size_t ws_bytes, float sm_scale, int32_t* status, uint64_t wait_ns,
                              cudaStream_t st) {
-  if (g.V > MAX_VIEWS || blk * (Hq / g.Hkv) > MAX_ROWS) return cudaErrorNotSupported;
-  const size_t units = (size_t)g.C * g.Hkv;
+  if (g.V > MAX_VIEWS || Hq / g.Hkv > MAX_ROWS) return cudaErrorNotSupported;
+  const int RH = row_halves(Hq, g.Hkv, blk);
+  const size_t units = (size_t)g.C * g.Hkv * RH;
   if (units == 0) return cudaSuccess;
   CUtensorMap tk, tv, tq;
   cudaError_t e = make_kv_tmaps(g, k, vt, BN, g.d, &tk, &tv);
   if (e != cudaSuccess) return e;
   {
     // block queries [C * blk tokens][Hq][d] bf16: a box is 64 columns of the
-    // G heads of one kv head for the blk tokens, i.e. the block rows (token, head)
+    // G heads of one kv head for the tokens of one row half, i.e. its block
+    // rows (token, head)
     const int G = Hq / g.Hkv;
+    const int box_tok = RH > 1 ? MAX_ROWS / G : blk;
     cuuint64_t dims[3] = {(cuuint64_t)g.d, (cuuint64_t)Hq, (cuuint64_t)g.C * blk};
     cuuint64_t strides[2] = {(cuuint64_t)g.d * 2, (cuuint64_t)Hq * g.d * 2};
-    cuuint32_t box[3] = {64, (cuuint32_t)G, (cuuint32_t)blk};
+    cuuint32_t box[3] = {64, (cuuint32_t)G, (cuuint32_t)box_tok};
     cuuint32_t es[3] = {1, 1, 1};
     auto fn = tmap_encode_fn();
     if (!fn) return cudaErrorNotSupported;
@@ -829,13 +847,16 @@ cudaError_t launch_verify_tc(const Geom& g, int Hq, int blk, const int32_t* tail
            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
-  const VerifyPlan pl = verify_plan(g);
+  const VerifyPlan pl = verify_plan(g, RH);
   VerifyParams p;
   p.g = g;
   p.Hq = Hq;
   p.G = Hq / g.Hkv;
   p.blk = blk;
   p.R = blk * p.G;
+  p.RH = RH;
+  p.RU = min(p.R, MAX_ROWS);
+  p.TQH = RH > 1 ? MAX_ROWS / p.G : blk;
   p.TM = pl.TM;
   p.W = pl.W;
   p.P_max = pl.P_max;
@@ -844,7 +865,7 @@ cudaError_t launch_verify_tc(const Geom& g, int Hq, int blk, const int32_t* tail
   p.out = static_cast<uint16_t*>(out);
   const size_t need = verify_ws_bytes(g, Hq, blk);
   if (ws_bytes < need || (need && !ws)) return cudaErrorInvalidValue;
-  const size_t n_rows = units * p.P_max * p.R;
+  const size_t n_rows = units * p.P_max * p.RU;
   p.ws_count = static_cast<int*>(ws);
   p.ws_o = need ? reinterpret_cast<float*>(static_cast<char*>(ws) + (units * 4 + 255) / 256 * 256) : nullptr;
   p.ws_ml = need ? p.ws_o + n_rows * g.d : nullptr;

@@ -169,6 +169,34 @@ def test_verify_full_block_rows_uneven_tails():
     assert pair.cache.device_status() == 0
 
 
+@pytest.mark.parametrize("B", [1, 8, 64])
+def test_verify_17_query_block(B):
+    """A 17-query block (the last accepted token + 16 drafts): 68 block rows
+    per kv head, taken as two row halves (64 + 4) that each stream the plane's
+    keys; accept lengths up to 16."""
+    w = W["alpamayo_verify"].with_(C=B, blk=17)
+    watch = list(range(B)) if B <= 8 else [0, 1, 31, 62, 63]
+    pair = Pair(w, "b17_%d" % B, watch=watch)
+    pair.fill()
+    pair.insert()
+    pair.set_tail(w.tail_len)
+    q, k, v = synth.verify_block(w, pair.tag)
+    target, draft, planted = synth.planted_ids(B, w.blk, pair.tag)
+    tail = torch.full((B,), w.tail_len, dtype=torch.int32, device="cuda")
+    out, acc, nxt = skv.stream_attn_verify(
+        pair.cache, tail, to_dev(q), to_dev(k), to_dev(v), w.sm_scale,
+        target_ids=torch.from_numpy(target).cuda(), draft_ids=torch.from_numpy(draft).cuda())
+    got = bf16_dev_to_f64(out)
+    acc, nxt = acc.cpu().numpy(), nxt.cpu().numpy()
+    for c in watch:
+        want, _ = O.stream_verify(pair.win[c], q[c], k[c], v[c], w.theta, w.sm_scale)
+        assert_close(got[c], want, "17-query verify B=%d cache %d" % (B, c))
+    for c in range(B):
+        a, n = O.accept_length(target[c], draft[c])
+        assert acc[c] == a == planted[c] and nxt[c] == n
+    assert pair.cache.device_status() == 0
+
+
 def test_verify_tiny_and_tail_advance():
     """Two verify rounds; the caller advances tail_len by accept_len + 1."""
     w = W["tiny"].with_(C=3, blk=9)
