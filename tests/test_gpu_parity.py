@@ -197,6 +197,42 @@ def test_verify_17_query_block(B):
     assert pair.cache.device_status() == 0
 
 
+# Degenerate and ragged geometries: no prefix, one view of one frame,
+# one-token frames, MHA (G = 1), eight query heads per kv head (a 9-query
+# block is then 72 rows: two row halves), frames and prefixes that fill no
+# tile evenly.
+DEGENERATE = [
+    # name, P, V, F, T, Hq, Hkv, d
+    ("no_prefix", 0, 2, 3, 40, 8, 2, 64),
+    ("one_view_one_frame", 16, 1, 1, 64, 8, 8, 128),
+    ("mha_ragged", 7, 3, 2, 33, 4, 4, 128),
+    ("gqa8", 12, 2, 2, 50, 64, 8, 128),
+    ("one_token_frames", 5, 3, 4, 1, 8, 2, 64),
+]
+
+
+@pytest.mark.parametrize("geo", DEGENERATE, ids=[g[0] for g in DEGENERATE])
+def test_degenerate_geometries(geo):
+    name, P, V, F, T, Hq, Hkv, d = geo
+    w = synth.Workload(name, P=P, V=V, F=F, T=T, Hq=Hq, Hkv=Hkv, d=d, theta=1e4, C=2,
+                       sm_scale=1.0 / np.sqrt(d), tail_cap=32, tail_len=5, blk=9)
+    pair = Pair(w, "dg")
+    pair.fill()
+    for _ in range(2):          # the ring wraps (F = 1: every insert replaces the frame)
+        pair.insert()
+    pair.check_ring()
+    _prefill_check(pair, "dg")
+    pair.set_tail(w.tail_len)
+    q, k, v = synth.verify_block(w, pair.tag)
+    tail = torch.full((w.C,), w.tail_len, dtype=torch.int32, device="cuda")
+    out, _, _ = skv.stream_attn_verify(pair.cache, tail, to_dev(q), to_dev(k), to_dev(v), w.sm_scale)
+    got = bf16_dev_to_f64(out)
+    for c in range(w.C):
+        want, _ = O.stream_verify(pair.win[c], q[c], k[c], v[c], w.theta, w.sm_scale)
+        assert_close(got[c], want, "%s verify cache %d" % (name, c))
+    assert pair.cache.device_status() == 0
+
+
 def test_verify_tiny_and_tail_advance():
     """Two verify rounds; the caller advances tail_len by accept_len + 1."""
     w = W["tiny"].with_(C=3, blk=9)
