@@ -212,6 +212,22 @@ def stream_prefill(win: StreamWindow, q_new, theta, sm_scale, rows=None):
     return attention_rows(q_new[rows], q_pos, k_bits, v_bits, k_pos, theta, sm_scale)
 
 
+def _block_after_tail(win: StreamWindow, blk_q, blk_k, blk_v, theta, sm_scale):
+    """Tokens appended after the window's tail, as queries: token j sits at
+    logical index n_visual + tail_len + j and sees the prefix, all frames, the
+    whole tail and block tokens 0..j.  blk_q [n][Hq][d], blk_k/blk_v
+    [n][Hkv][d].  Returns (O [n][Hq][d], LSE [n][Hq])."""
+    k_bits, v_bits = win.logical_kv(with_tail=True)
+    base = k_bits.shape[0]
+    blk = np.asarray(blk_q).shape[0]
+    k_all = np.concatenate([k_bits, np.asarray(blk_k, np.uint16)], axis=0)
+    v_all = np.concatenate([v_bits, np.asarray(blk_v, np.uint16)], axis=0)
+    k_pos = np.arange(k_all.shape[0])
+    q_pos = base + np.arange(blk)
+    return attention_rows(np.asarray(blk_q, np.uint16), q_pos, k_all, v_all, k_pos,
+                          theta, sm_scale)
+
+
 def stream_verify(win: StreamWindow, blk_q, blk_k, blk_v, theta, sm_scale):
     """Speculative-verify block ([FD-blog] 4.2 steps 1-2; [VFlash] "03 ·
     Generalist decoding": the target checks a whole drafted block in one
@@ -222,15 +238,42 @@ def stream_verify(win: StreamWindow, blk_q, blk_k, blk_v, theta, sm_scale):
     and block tokens 0..j.  blk_q [blk][Hq][d], blk_k/blk_v [blk][Hkv][d].
     Returns (O [blk][Hq][d], LSE [blk][Hq]).
     """
-    k_bits, v_bits = win.logical_kv(with_tail=True)
-    base = k_bits.shape[0]
-    blk = np.asarray(blk_q).shape[0]
-    k_all = np.concatenate([k_bits, np.asarray(blk_k, np.uint16)], axis=0)
-    v_all = np.concatenate([v_bits, np.asarray(blk_v, np.uint16)], axis=0)
-    k_pos = np.arange(k_all.shape[0])
-    q_pos = base + np.arange(blk)
-    return attention_rows(np.asarray(blk_q, np.uint16), q_pos, k_all, v_all, k_pos,
-                          theta, sm_scale)
+    return _block_after_tail(win, blk_q, blk_k, blk_v, theta, sm_scale)
+
+
+def stream_prefill_tail(win: StreamWindow, tail_q, tail_k, tail_v, theta, sm_scale):
+    """Trajectory / text tokens after the views as queries ([FD-blog] 3.2
+    "View-Major Ordering": the trailing trajectory and text tokens see every
+    view and are causal among themselves; with the newest frames they are the
+    only new queries of a step).
+
+    The n tokens follow the window's current tail: token j sits at logical
+    index n_visual + tail_len + j and sees everything before it plus tokens
+    0..j of its own span -- the same rows a verify block of n tokens computes.
+    tail_q [n][Hq][d], tail_k/tail_v [n][Hkv][d].  Returns (O, LSE).  The
+    caller appends tail_k/tail_v to the window's tail afterwards.
+    """
+    return _block_after_tail(win, tail_q, tail_k, tail_v, theta, sm_scale)
+
+
+def stream_window(win: StreamWindow, q_win, theta, sm_scale, rows=None):
+    """Every token of the window as a query: the first window of a stream,
+    which only fills the cache ([FD-blog] 11 "Implementation Map": the first
+    streaming window returns no trajectory), or a full re-encode.
+
+    q_win [N][Hq][d] pre-RoPE bits in logical order -- the prefix, then view
+    0's frames oldest to newest, then view 1's, ... -- N = P + V*F*T.  Token i
+    sits at position i and sees keys 0..i ([FD-blog] 3.2: the prefix is seen
+    by every frame, a view sees the earlier views, its own older frames and
+    its own frame causally).  The tail follows the window and is not
+    visible.  `rows` optionally restricts the computation to a subset of
+    tokens.  Returns (O, LSE) for the selected rows.
+    """
+    q_win = np.asarray(q_win, dtype=np.uint16)
+    k_bits, v_bits = win.logical_kv(with_tail=False)
+    n = k_bits.shape[0]
+    rows = np.arange(n) if rows is None else np.asarray(rows)
+    return attention_rows(q_win[rows], rows, k_bits, v_bits, np.arange(n), theta, sm_scale)
 
 
 def accept_length(target_ids, draft_ids):

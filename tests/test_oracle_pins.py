@@ -471,6 +471,118 @@ def test_verify_rows_are_causal_within_block():
 
 
 # --------------------------------------------------------------------------
+# the whole window as queries (first window) and tail tokens as queries
+
+def _causal_sdpa(q_bits, k_bits, v_bits, theta, scale):
+    """torch SDPA fp64 with its own causal mask (is_causal): query i sees keys
+    0..i of a sequence whose positions are 0..N-1."""
+    torch = pytest.importorskip("torch")
+    import torch.nn.functional as Fn
+    pos = np.arange(k_bits.shape[0])
+    qf, kf, vf = O.bf16_to_f64(q_bits), O.bf16_to_f64(k_bits), O.bf16_to_f64(v_bits)
+    qr = np.stack([_rope_complex(qf[:, h], pos, theta) for h in range(qf.shape[1])], 0)
+    kr = np.stack([_rope_complex(kf[:, h], pos, theta) for h in range(kf.shape[1])], 0)
+    vr = np.transpose(vf, (1, 0, 2))
+    o = Fn.scaled_dot_product_attention(torch.from_numpy(qr)[None], torch.from_numpy(kr)[None],
+                                        torch.from_numpy(np.ascontiguousarray(vr))[None],
+                                        is_causal=True, scale=scale, enable_gqa=True)
+    return np.transpose(o[0].numpy(), (1, 0, 2))
+
+
+@pytest.mark.parametrize("n_inserts", [2, 5])
+def test_window_is_causal_attention_over_the_listing(n_inserts):
+    """First window (n_inserts = F) and a rotated ring (F + 3): every token a
+    query is plain causal attention over the logical sequence."""
+    w = synth.WORKLOADS["tiny"]
+    win = _tiny_window(w, n_inserts, "win%d" % n_inserts)
+    q = synth.normal_bf16((win.n_visual, w.Hq, w.d), "winq", n_inserts)
+    got, lse = O.stream_window(win, q, w.theta, w.sm_scale)
+    k, v = win.logical_kv(with_tail=False)
+    want = _causal_sdpa(q, k, v, w.theta, w.sm_scale)
+    np.testing.assert_allclose(got, want, rtol=1e-10, atol=1e-12)
+    assert got.shape == (win.n_visual, w.Hq, w.d) and lse.shape == (win.n_visual, w.Hq)
+
+
+def test_window_first_token_sees_only_itself():
+    """Token 0 has a single visible key, so its output is that key's value
+    exactly and its LSE is its own scaled score."""
+    w = synth.WORKLOADS["tiny"]
+    win = _tiny_window(w, w.F, "one")
+    q = synth.normal_bf16((win.n_visual, w.Hq, w.d), "oneq")
+    got, lse = O.stream_window(win, q, w.theta, w.sm_scale, rows=np.array([0]))
+    G = w.Hq // w.Hkv
+    v0 = O.bf16_to_f64(win.prefix_v[0])
+    for h in range(w.Hq):
+        np.testing.assert_array_equal(got[0, h], v0[h // G])
+        s = float(O.bf16_to_f64(q[0, h]) @ O.bf16_to_f64(win.prefix_k[0, h // G])) * w.sm_scale
+        assert abs(lse[0, h] - s) < 1e-12     # position 0: the rotation is the identity
+
+
+def test_window_newest_frame_rows_equal_prefill():
+    """The window's rows of each view's newest frame are the streaming
+    prefill's rows: same positions, same visible keys."""
+    w = synth.WORKLOADS["tiny"]
+    win = _tiny_window(w, w.F + 1, "same")
+    qn = synth.frame_q(w, w.F, "same")[0]
+    q = synth.normal_bf16((win.n_visual, w.Hq, w.d), "sameq")
+    rows = np.array([win.new_frame_index(v, t) for v in range(w.V) for t in range(w.T)])
+    q[rows] = qn
+    a, la = O.stream_window(win, q, w.theta, w.sm_scale, rows=rows)
+    b, lb = O.stream_prefill(win, qn, w.theta, w.sm_scale)
+    np.testing.assert_allclose(a, b, rtol=1e-13, atol=1e-14)
+    np.testing.assert_allclose(la, lb, rtol=1e-13, atol=1e-14)
+
+
+def test_window_earlier_tokens_ignore_later_frames():
+    """Changing view 1's newest frame leaves every token before it unchanged,
+    bit for bit, and changes that frame's own rows."""
+    w = synth.WORKLOADS["tiny"]
+    win_a = _tiny_window(w, w.F, "late")
+    win_b = _tiny_window(w, w.F, "late")
+    k, v = win_b.views[1][-1]
+    win_b.views[1][-1] = (k ^ np.uint16(0x0040), v ^ np.uint16(0x0040))
+    q = synth.normal_bf16((win_a.n_visual, w.Hq, w.d), "lateq")
+    a, _ = O.stream_window(win_a, q, w.theta, w.sm_scale)
+    b, _ = O.stream_window(win_b, q, w.theta, w.sm_scale)
+    first = win_a.new_frame_index(1, 0)
+    np.testing.assert_array_equal(a[:first], b[:first])
+    assert np.abs(a[first:] - b[first:]).max() > 0
+
+
+def test_tail_prefill_vs_sdpa():
+    w = synth.WORKLOADS["tiny"]
+    win = _tiny_window(w, w.F + 2, "tp")
+    tk, tv = synth.tail_kv(w, 4, "tp")
+    win.set_tail(tk[0], tv[0])
+    n = 11
+    q = synth.normal_bf16((n, w.Hq, w.d), "tpq")
+    k = synth.normal_bf16((n, w.Hkv, w.d), "tpk")
+    v = synth.normal_bf16((n, w.Hkv, w.d), "tpv")
+    got, _ = O.stream_prefill_tail(win, q, k, v, w.theta, w.sm_scale)
+    base = win.n_visual + 4
+    want = _full_sequence_sdpa(win, q, base + np.arange(n), k, v, w.sm_scale, w.theta)
+    np.testing.assert_allclose(got, want, rtol=1e-10, atol=1e-12)
+
+
+def test_tail_prefill_at_once_equals_token_by_token():
+    """Causal within the span: n tokens in one call give the rows that n
+    one-token calls give when each call's K/V is appended to the tail before
+    the next."""
+    w = synth.WORKLOADS["tiny"]
+    win = _tiny_window(w, w.F, "inc")
+    n = 6
+    q = synth.normal_bf16((n, w.Hq, w.d), "incq")
+    k = synth.normal_bf16((n, w.Hkv, w.d), "inck")
+    v = synth.normal_bf16((n, w.Hkv, w.d), "incv")
+    whole, lw = O.stream_prefill_tail(win, q, k, v, w.theta, w.sm_scale)
+    for j in range(n):
+        one, lo = O.stream_prefill_tail(win, q[j:j + 1], k[j:j + 1], v[j:j + 1], w.theta, w.sm_scale)
+        np.testing.assert_allclose(one[0], whole[j], rtol=1e-12, atol=1e-13)
+        np.testing.assert_allclose(lo[0], lw[j], rtol=1e-12, atol=1e-13)
+        win.set_tail(np.concatenate([win.tail_k, k[j:j + 1]]), np.concatenate([win.tail_v, v[j:j + 1]]))
+
+
+# --------------------------------------------------------------------------
 # accept length
 
 def test_accept_page_example():
