@@ -58,6 +58,18 @@ def prefill_flop(w) -> float:
     return 4.0 * w.d * w.Hq * w.C * prefill_pairs(w)
 
 
+def window_flop(w) -> float:
+    """Every window token a query: token i sees keys 0..i."""
+    n = w.n_window
+    return 4.0 * w.d * w.Hq * w.C * n * (n + 1) / 2
+
+
+def tail_flop(w, n: int, tail_len: int = 0) -> float:
+    """n tail tokens after tail_len tail rows: token j sees the window, the
+    tail_len rows and tokens 0..j."""
+    return 4.0 * w.d * w.Hq * w.C * (n * (w.n_window + tail_len) + n * (n + 1) / 2)
+
+
 def verify_bytes(w) -> float:
     """Per launch: K and V of every visible key once per (cache, kv head),
     the block's Q in and O out, the block K/V read and written to the tail."""
@@ -228,8 +240,8 @@ def run_reference(args, rank, world):
 
 def run_only(args):
     """One kernel alone on a reduced case (for ncu captures): scale-up
-    geometry with --layers caches for prefill/insert, the verify workload
-    with batch --layers for verify."""
+    geometry with --layers caches for prefill/insert/window/tail, the verify
+    workload with batch --layers for verify."""
     import torch
     from streaming_kv_cache_gb300 import build as B
     B.build()
@@ -242,6 +254,8 @@ def run_only(args):
         return (torch.randn(shape, generator=gen, device=dev) * scale).to(torch.bfloat16)
 
     w = (VERIFY_W if args.only == "verify" else PREFILL_W).with_(C=args.layers)
+    if args.only == "tail":
+        w = w.with_(tail_cap=max(w.tail_cap, args.tail_n))
     if args.only == "verify" and args.blk:
         w = w.with_(blk=args.blk)
     cache = skv.StreamCache(w.C, w.P, w.V, w.F, w.T, w.Hkv, w.d, w.theta, tail_cap=w.tail_cap)
@@ -254,6 +268,21 @@ def run_only(args):
         out = torch.empty_like(q)
         fn = lambda: skv.stream_attn_prefill(cache, q, w.sm_scale, out=out)
         work = prefill_flop(w) / 1e12
+        unit = "TFLOP/s"
+    elif args.only == "window":
+        q = randn((w.C, w.n_window, w.Hq, w.d), w.q_scale)
+        out = torch.empty_like(q)
+        fn = lambda: skv.stream_attn_window(cache, q, w.sm_scale, out=out)
+        work = window_flop(w) / 1e12
+        unit = "TFLOP/s"
+    elif args.only == "tail":
+        n = args.tail_n
+        q = randn((w.C, n, w.Hq, w.d), w.q_scale)
+        kt = randn((w.C, n, w.Hkv, w.d))
+        tail = torch.zeros((w.C,), dtype=torch.int32, device=dev)
+        out = torch.empty_like(q)
+        fn = lambda: skv.stream_attn_prefill_tail(cache, tail, q, kt, kt, w.sm_scale, out=out)
+        work = tail_flop(w, n) / 1e12
         unit = "TFLOP/s"
     elif args.only == "insert":
         fn = lambda: skv.kv_stream_insert(cache, k_new, k_new)
@@ -308,10 +337,12 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["prefill", "verify", "insert"], default=None,
+    ap.add_argument("--only", choices=["prefill", "verify", "insert", "window", "tail"], default=None,
                     help="profiling aid: time one kernel alone on a reduced case and print its ms")
     ap.add_argument("--layers", type=int, default=4,
                     help="layer caches (prefill/insert) or batch (verify) of the --only case")
+    ap.add_argument("--tail-n", type=int, default=128,
+                    help="tail tokens of the --only tail case (after an empty tail)")
     ap.add_argument("--blk", type=int, default=None,
                     help="verify block size of the --only verify case (default: the workload's 9)")
     args = ap.parse_args()

@@ -202,6 +202,52 @@ int kv_stream_insert_noalloc(const skv_cache* cache, const void* k_new, const vo
 int stream_attn_prefill(const skv_cache* cache, int32_t n_q_head, const void* q_new, void* out,
                         float* lse, float sm_scale, void* stream);
 
+/*
+ * stream_attn_prefill_tail -- the trajectory / text tokens that follow the
+ * views, as queries (blog section 3.2: they see every view and are causal
+ * among themselves; with the newest frames they are a step's only new
+ * queries).  Runs on the same tensor-core kernel as stream_attn_prefill.
+ *
+ * Tail token j (j < n_tok) of cache c sits at logical index
+ * P + V*F*T + tail_len[c] + j.  The call
+ *  1. writes the tokens' pre-RoPE K/V into tail rows tail_len[c] + j;
+ *  2. attends each token over the prefix, all frames, the tail
+ *     [0, tail_len[c]) and tokens 0..j of its own span.
+ * The caller then advances tail_len[c] by n_tok.
+ *
+ * tail_len: device int32 [C], tokens already in the tail (0 at the start of
+ *           a step).
+ * q_tail:   device bf16 [C][n_tok][Hq][d]; k_tail, v_tail: [C][n_tok][Hkv][d].
+ * out:      device bf16 [C][n_tok][Hq][d].
+ * lse:      device fp32 [C][Hq][n_tok] or NULL.
+ * Needs 1 <= n_tok <= tail_cap, Hq % Hkv == 0 and 128 % (Hq/Hkv) == 0.
+ * tail_len[c] < 0 sets SKV_DEV_BAD_TAIL, tail_len[c] + n_tok > tail_cap sets
+ * SKV_DEV_TAIL_OVERFLOW; that cache is then neither written nor attended.
+ */
+int stream_attn_prefill_tail(const skv_cache* cache, int32_t n_q_head, int32_t n_tok,
+                             const int32_t* tail_len, const void* q_tail, const void* k_tail,
+                             const void* v_tail, void* out, float* lse, float sm_scale,
+                             void* stream);
+
+/*
+ * stream_attn_window -- every token of the window as a query: the first
+ * window of a stream, which only fills the cache (blog section 11), or a
+ * full re-encode.  Call it once the window is full (F inserts).
+ *
+ * Window token i (i < N = P + V*F*T) is the token at logical index i: the
+ * prefix, then view 0's frames oldest to newest, then view 1's, ...  It sees
+ * every key whose logical index is at most i (never the tail); queries and
+ * keys are rotated at their logical positions in the kernel.  The ring may
+ * have any head: frame f of view v is read from slot (head + f) mod F.
+ *
+ * q_win: device bf16 [C][N][Hq][d], pre-RoPE, in logical order.
+ * out:   device bf16 [C][N][Hq][d].
+ * lse:   device fp32 [C][Hq][N] or NULL.
+ * Needs Hq % Hkv == 0 and 128 % (Hq/Hkv) == 0.
+ */
+int stream_attn_window(const skv_cache* cache, int32_t n_q_head, const void* q_win, void* out,
+                       float* lse, float sm_scale, void* stream);
+
 /* Bytes of device workspace stream_attn_verify needs for this geometry. */
 size_t skv_verify_workspace_bytes(const skv_cache* cache, int32_t n_q_head, int32_t blk);
 

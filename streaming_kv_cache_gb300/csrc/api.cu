@@ -151,7 +151,64 @@ int stream_attn_prefill(const skv_cache* cache, int32_t n_q_head, const void* q_
   if (lse && ((uintptr_t)lse & 3u)) return SKV_ERR_INVALID;
   if ((rc = check_device())) return rc;
   const skv::Geom g = skv::geom_of(*cache);
-  cudaError_t e = skv::launch_prefill_tc(g, n_q_head, q_new, out, lse, cache->k, cache->vt, cache->rope,
+  skv::PrefillQuery qs{};
+  qs.nf = 1;                        // the newest frame of every view
+  qs.NQ = g.V * g.T;
+  cudaError_t e = skv::launch_prefill_tc(g, n_q_head, qs, q_new, out, lse, cache->k, cache->vt, cache->rope,
+                                         cache->head, sm_scale, cache->status, cache->wait_ns,
+                                         (cudaStream_t)stream);
+  return e == cudaSuccess ? SKV_OK : cuda_fail(e);
+}
+
+int stream_attn_prefill_tail(const skv_cache* cache, int32_t n_q_head, int32_t n_tok,
+                             const int32_t* tail_len, const void* q_tail, const void* k_tail,
+                             const void* v_tail, void* out, float* lse, float sm_scale,
+                             void* stream) {
+  int rc = check_cache(cache);
+  if (rc) return rc;
+  if (n_q_head < 1 || n_q_head % cache->n_kv_head) return SKV_ERR_INVALID;
+  if (n_tok < 1 || n_tok > cache->tail_cap) return SKV_ERR_INVALID;
+  if (128 % (n_q_head / cache->n_kv_head)) return SKV_ERR_UNSUPPORTED;
+  if (!(sm_scale > 0.f) || sm_scale != sm_scale) return SKV_ERR_INVALID;
+  if (cache->n_cache == 0) return SKV_OK;
+  if (!tail_len || !q_tail || !k_tail || !v_tail || !out) return SKV_ERR_INVALID;
+  if (!aligned16(q_tail) || !aligned16(k_tail) || !aligned16(v_tail) || !aligned16(out))
+    return SKV_ERR_INVALID;
+  if (((uintptr_t)tail_len & 3u) || (lse && ((uintptr_t)lse & 3u))) return SKV_ERR_INVALID;
+  if ((rc = check_device())) return rc;
+  const skv::Geom g = skv::geom_of(*cache);
+  cudaStream_t st = (cudaStream_t)stream;
+  // the tokens' K/V into the tail, then their attention (same stream order)
+  cudaError_t e = skv::launch_write_rows(g, cache->k, cache->vt, k_tail, v_tail, 1, n_tok, 2, 0,
+                                         cache->head, cache->sync, tail_len, cache->status, st);
+  if (e != cudaSuccess) return cuda_fail(e);
+  skv::PrefillQuery qs{};
+  qs.n_tail = n_tok;
+  qs.tail_len = tail_len;
+  qs.NQ = n_tok;
+  e = skv::launch_prefill_tc(g, n_q_head, qs, q_tail, out, lse, cache->k, cache->vt, cache->rope, cache->head,
+                             sm_scale, cache->status, cache->wait_ns, st);
+  return e == cudaSuccess ? SKV_OK : cuda_fail(e);
+}
+
+int stream_attn_window(const skv_cache* cache, int32_t n_q_head, const void* q_win, void* out,
+                       float* lse, float sm_scale, void* stream) {
+  int rc = check_cache(cache);
+  if (rc) return rc;
+  if (n_q_head < 1 || n_q_head % cache->n_kv_head) return SKV_ERR_INVALID;
+  if (128 % (n_q_head / cache->n_kv_head)) return SKV_ERR_UNSUPPORTED;
+  if (!(sm_scale > 0.f) || sm_scale != sm_scale) return SKV_ERR_INVALID;
+  if (cache->n_cache == 0) return SKV_OK;
+  if (!q_win || !out || !aligned16(q_win) || !aligned16(out)) return SKV_ERR_INVALID;
+  if (lse && ((uintptr_t)lse & 3u)) return SKV_ERR_INVALID;
+  if ((rc = check_device())) return rc;
+  const skv::Geom g = skv::geom_of(*cache);
+  skv::PrefillQuery qs{};
+  qs.nf = g.F;                      // every frame of every view, and the prefix
+  qs.prefix = true;
+  qs.NQ = g.n_visual();
+  qs.q_view0 = g.P;
+  cudaError_t e = skv::launch_prefill_tc(g, n_q_head, qs, q_win, out, lse, cache->k, cache->vt, cache->rope,
                                          cache->head, sm_scale, cache->status, cache->wait_ns,
                                          (cudaStream_t)stream);
   return e == cudaSuccess ? SKV_OK : cuda_fail(e);

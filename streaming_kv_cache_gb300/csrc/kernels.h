@@ -19,9 +19,22 @@ cudaError_t launch_write_rows(const Geom& g, void* k, void* vt, const void* k_sr
 
 cudaError_t launch_rope_table(float* tab, int n_pos, int d, double theta, cudaStream_t st);
 
-cudaError_t launch_prefill_tc(const Geom& g, int Hq, const void* q, void* out, float* lse, const void* k,
-                              const void* vt, const float* rope, const int32_t* head, float sm_scale,
-                              int32_t* status, uint64_t wait_ns, cudaStream_t st);
+// The query tokens of one prefill launch, the same for every cache; a
+// cache's rows of q / out / lse hold NQ tokens.
+struct PrefillQuery {
+  int nf;                   // frames per view that are queries: 0, 1 (the newest) or F (all)
+  bool prefix;              // the prefix tokens are queries
+  int n_tail;               // tail tokens that are queries (they follow tail_len[c] tail rows)
+  const int32_t* tail_len;  // [C] on the device; needed when n_tail > 0
+  int NQ;                   // query tokens per cache
+  int q_view0;              // token of view 0's first queried frame; view v, queried frame i at
+                            // q_view0 + (v * nf + i) * T
+  int q_tail0;              // token of the first tail query; prefix token j at j
+};
+
+cudaError_t launch_prefill_tc(const Geom& g, int Hq, const PrefillQuery& qs, const void* q, void* out, float* lse,
+                              const void* k, const void* vt, const float* rope, const int32_t* head,
+                              float sm_scale, int32_t* status, uint64_t wait_ns, cudaStream_t st);
 
 cudaError_t launch_verify_tc(const Geom& g, int Hq, int blk, const int32_t* tail_len, const void* q, void* out,
                              const void* k, const void* vt, const float* rope, const int32_t* head,

@@ -6,9 +6,16 @@
 // newest frame of each view becomes queries; it sees the system prefix, the
 // earlier views, its own view's older frames and its own frame causally;
 // keys are cached pre-RoPE and rotated at their current logical position.
+// The same kernel takes the other query sets of the method, as segments of
+// consecutive logical positions: the trajectory / text tokens after the views
+// (section 3.2: they see every view and are causal among themselves) and
+// every token of the window (section 11: the first window only fills the
+// cache).  A query sees exactly the keys whose logical index is not above its
+// own; in physical rows that is a prefix of the rows minus, for a frame of a
+// view, the rest of that view's ring after the query (at most two runs).
 //
-// A cluster of two CTAs handles one (cache, kv head, view, 4*TQ new-frame
-// tokens); each CTA owns 2 x 128 query rows that pack TQ = 128/G tokens x the
+// A cluster of two CTAs handles one (cache, kv head, segment, 4*TQ tokens);
+// each CTA owns 2 x 128 query rows that pack TQ = 128/G tokens x the
 // G query heads sharing the kv head (GQA).  Both CTAs walk the same list of
 // 128-key tiles in physical (ring) order -- softmax does not depend on key
 // order, so only positions and the mask need logical indices.  Each CTA
@@ -79,7 +86,10 @@ struct Layout {
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
   static constexpr int HEAD_OFF = MISC_OFF + 64;     // ring heads of this cache (<= MAX_VIEWS)
   static constexpr int TILE_OFF = HEAD_OFF + MAX_VIEWS * 4;
-  static constexpr int BYTES = TILE_OFF + MAX_TILES * 4;
+  // per softmax row: the second run of its mask (a2, n2), its output row
+  // (-1: none) and its LSE index
+  static constexpr int MASK_OFF = TILE_OFF + MAX_TILES * 4;
+  static constexpr int BYTES = MASK_OFF + 4 * 2 * BM * 4;
   static constexpr int ALLOC = BYTES + 1024;   // slack for 1024-byte alignment
 };
 
@@ -103,7 +113,17 @@ static_assert(Layout<128>::NBAR >= B_COUNT && Layout<64>::NBAR >= B_COUNT, "barr
 
 struct PrefillParams {
   Geom g;
-  int Hq, G, TQ, pairs;   // pairs of CTAs per view (each CTA: 2*TQ tokens)
+  int Hq, G, TQ;
+  // query segments of every cache and the work items they make (blocks of
+  // 4*TQ tokens, one CTA pair each), in the order the items of a (cache, kv
+  // head) plane run: the tail block, the views' frames, the prefix
+  int nbt, n_tail;        // tail blocks and tail query tokens
+  int nf, nbf;            // frames per view that are queries (0, 1 = newest, F) and blocks per frame
+  int nbp;                // prefix blocks (0: the prefix is not queried)
+  int items;              // items per plane: nbt + V*nf*nbf + nbp
+  int NQ;                 // query tokens per cache in q / out / lse
+  int q_view0, q_tail0;   // a cache's first query token of the view frames and of the tail block
+  const int32_t* tail_len;  // [C] tail rows the tail block follows
   const uint16_t* q;
   uint16_t* out;
   float* lse;
@@ -115,6 +135,22 @@ struct PrefillParams {
 };
 
 // SW: compiled for a wait limit under the suspend hint (see tc::bounded_wait)
+// Keys of view v's ring that a query at logical frame f, token t (frame f in
+// ring slot `slot`) may not see: the later tokens of its own frame and the
+// view's later frames, a cyclic run of the ring starting just after the
+// query's row, returned as at most two runs of physical rows [a1, a1 + n1)
+// and [a2, a2 + n2).
+__device__ __forceinline__ void ring_hole(const Geom& g, int v, int f, int slot, int t, int& a1, int& n1,
+                                          int& a2, int& n2) {
+  const int FT = g.F * g.T, base = g.P + v * FT;
+  const int o = slot * g.T + t + 1;                        // 1 .. FT
+  const int len = (g.F - 1 - f) * g.T + (g.T - 1 - t);
+  n1 = min(len, FT - o);
+  a1 = base + o;
+  n2 = len - n1;
+  a2 = base;
+}
+
 template <int D, bool SW>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
@@ -129,6 +165,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
   int* s_ntiles = reinterpret_cast<int*>(smem + L::MISC_OFF + 8);
   int* s_tiles = reinterpret_cast<int*>(smem + L::TILE_OFF);
   int* s_head = reinterpret_cast<int*>(smem + L::HEAD_OFF);
+  int* s_mask = reinterpret_cast<int*>(smem + L::MASK_OFF);
+  int* s_wrap = reinterpret_cast<int*>(smem + L::MISC_OFF + 12);   // 1: some row's mask has a second run
 
   const Geom& g = p.g;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -136,19 +174,47 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
   // barriers in the even CTA, addressed across the cluster
   auto bar_even = [&](int i) { return tc::map_to_cta(bar(i), 0); };
 
-  // work item: the pairs of one (cache, kv head) are adjacent, so they run
-  // together and share that plane's K/V tiles through L2; inside a plane
-  // the later (heavier) views come first
+  // work item: the items of one (cache, kv head) are adjacent, so they run
+  // together and share that plane's K/V tiles through L2; inside a plane the
+  // heavier items come first: the tail block (it sees the whole window),
+  // then the frames, later views and frames first, then the prefix
   int w = blockIdx.x >> 1;
-  const int pc = w % p.pairs;      w /= p.pairs;
-  const int vq = g.V - 1 - (w % g.V);  w /= g.V;
-  const int h = w % g.Hkv;         w /= g.Hkv;
-  const int c = w;
-  const int t0 = (pc * 2 + (int)rank) * 2 * p.TQ;      // first token of this CTA
-  const int t_max = min(g.T, (pc + 1) * 4 * p.TQ) - 1;  // last token of the pair (shared tile list)
-  const int32_t* head_c = p.head + (size_t)c * g.V;
+  const int it = w % p.items;      w /= p.items;
+  const int h = w % g.Hkv;
+  const int c = w / g.Hkv;
   const int FT = g.F * g.T;
-  const int row_end = g.P + (vq + 1) * FT;         // keys beyond are later views / tail
+  int pc, n_seg, qoff, pos0, vq = -1, fq = 0, vmax = -1, bad = 0;
+  if (it < p.nbt) {                                // tail block
+    pc = it;
+    n_seg = p.n_tail;
+    qoff = p.q_tail0;
+    const int tl = p.tail_len[c];
+    bad = tl < 0 ? SKV_DEV_BAD_TAIL : (tl + p.n_tail > g.tail_cap ? SKV_DEV_TAIL_OVERFLOW : 0);
+    pos0 = g.n_visual() + max(tl, 0);
+    vmax = g.V - 1;
+  } else if (it < p.nbt + g.V * p.nf * p.nbf) {    // one frame of one view
+    int j = it - p.nbt;
+    pc = j % p.nbf;  j /= p.nbf;
+    const int fi = j % p.nf;
+    vq = g.V - 1 - j / p.nf;
+    fq = g.F - 1 - fi;
+    n_seg = g.T;
+    qoff = p.q_view0 + (vq * p.nf + (p.nf - 1 - fi)) * g.T;
+    pos0 = g.P + vq * FT + fq * g.T;
+    vmax = vq;
+  } else {                                         // prefix
+    pc = it - p.nbt - g.V * p.nf * p.nbf;
+    n_seg = g.P;
+    qoff = 0;
+    pos0 = 0;
+  }
+  const int t0 = (pc * 2 + (int)rank) * 2 * p.TQ;      // first token of this CTA
+  const int t_max = min(n_seg, (pc + 1) * 4 * p.TQ) - 1;  // last token of the pair (shared tile list)
+  const int32_t* head_c = p.head + (size_t)c * g.V;
+  // keys beyond are never visible to the item: later views and the tail for
+  // a frame; for the prefix and the tail (physical row = logical index) the
+  // rows after the item's last token
+  const int row_end = vq >= 0 ? g.P + (vq + 1) * FT : pos0 + t_max + 1;
   const int zc = c * g.Hkv + h;                    // (cache, kv head) plane of the tensor maps
   const uint64_t wait_ns = p.wait_ns;
 
@@ -164,34 +230,43 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
       }
       *s_abort = 0;
     }
-    // ring heads of views 0..vq, one lane per view
-    bool ok = true;
-    for (int v = lane; v <= vq; v += 32) {
+    // ring heads of the views whose rows the item reads, one lane per view
+    bool ok = bad == 0;
+    for (int v = lane; v <= vmax; v += 32) {
       const int hv = head_c[v];
       ok = ok && hv >= 0 && hv < g.F;
       s_head[v] = hv;
     }
     ok = __all_sync(0xffffffffu, ok);
     // tile list over physical key rows [0, row_end), skipping tiles made only
-    // of newest-frame rows that no query of the pair may see; 32 tiles per step
-    int n = 0;
+    // of ring rows that no query of the pair may see (the hole of its last
+    // token lies inside every other token's); 32 tiles per step
+    int n = 0, wrap = 0;
     if (ok) {
-      const int s_new = (head_c[vq] + g.F - 1) % g.F;
-      const int ns0 = g.P + (vq * g.F + s_new) * g.T;
-      const int inv_lo = ns0 + t_max + 1, inv_hi = ns0 + g.T;
+      int a1 = 0, n1 = 0, a2 = 0, n2 = 0;
+      if (vq >= 0) {
+        const int slot = (head_c[vq] + fq) % g.F;
+        ring_hole(g, vq, fq, slot, t_max, a1, n1, a2, n2);
+        // the first token's hole holds every other token's: if it has no
+        // second run, no row's mask has one
+        int u1, m1, u2, m2;
+        ring_hole(g, vq, fq, slot, pc * 4 * p.TQ, u1, m1, u2, m2);
+        wrap = m2 > 0;
+      }
       const int n_all = (row_end + BN - 1) / BN;
       for (int k0 = 0; k0 < n_all; k0 += 32) {
-        const int k = k0 + lane, r0 = k * BN;
-        const bool keep = k < n_all && !(r0 >= inv_lo && min(r0 + BN, row_end) <= inv_hi);
+        const int k = k0 + lane, r0 = k * BN, r1 = min(r0 + BN, row_end);
+        const bool keep = k < n_all && !(r0 >= a1 && r1 <= a1 + n1) && !(r0 >= a2 && r1 <= a2 + n2);
         const uint32_t ball = __ballot_sync(0xffffffffu, keep);
         if (keep) s_tiles[n + __popc(ball & ((1u << lane) - 1))] = r0;
         n += __popc(ball);
       }
     } else if (rank == 0 && lane == 0) {
-      set_status(p.status, SKV_DEV_BAD_HEAD);
+      set_status(p.status, bad ? bad : SKV_DEV_BAD_HEAD);
     }
     if (lane == 0) {
       *s_ntiles = n;
+      *s_wrap = wrap;
       tc::fence_barrier_init();
     }
   }
@@ -215,7 +290,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
         tc::prefetch_tmap(is_k ? &tmap_k : &tmap_v);
         if (is_k) {
           // both query tiles: rows (token, head) of kv head h, 64 columns per box
-          const int z0 = (c * g.V + vq) * g.T + t0;
+          const int z0 = c * p.NQ + qoff + t0;
           tc::mbar_arrive_expect_tx(bar(B_QLOAD), 2 * L::QT);
 #pragma unroll
           for (int i = 0; i < 2; ++i)
@@ -409,16 +484,33 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
     const int row = lg * 32 + lane;
     const int tok = t0 + i * p.TQ + row / p.G;
     const int gq = row % p.G;
-    const bool valid = tok < g.T;
+    const bool valid = tok < n_seg;
     const uint32_t t_lane = (uint32_t)(lg * 32) << 16;
     const uint32_t tS = tmem + t_lane + i * 128;
     const uint32_t tO = tmem + t_lane + 256 + i * 128;
-    int ns0 = 0;
+    // the keys this query sees: rows [0, row_end) minus [a1, a1 + n1) and
+    // [a2, a2 + n2) (rows past the segment's end act as its last token); the
+    // second run, when the ring has turned, waits in shared memory
+    int* my_mask = s_mask + i * BM + row;
+    const uint32_t mask_sa = sbase + L::MASK_OFF + 4u * (i * BM + row);
+    int a1 = 0, n1 = 0;
+    const bool wrap = *s_wrap != 0;
     if (nt > 0) {
-      const int s_new = (head_c[vq] + g.F - 1) % g.F;
-      ns0 = g.P + (vq * g.F + s_new) * g.T;
+      const int tq = min(tok, n_seg - 1);
+      int a2 = 0, n2 = 0;
+      if (vq < 0) {
+        a1 = pos0 + tq + 1;         // the later tokens of a prefix / tail span
+        n1 = row_end - a1;
+      } else {
+        ring_hole(g, vq, fq, (s_head[vq] + fq) % g.F, tq, a1, n1, a2, n2);
+      }
+      my_mask[0] = a2;
+      my_mask[2 * BM] = n2;
+      // output row (token, head) and LSE entry; both below 2^31 (checked at launch)
+      const int tok_row = c * p.NQ + qoff + tok;
+      my_mask[4 * BM] = valid ? tok_row * p.Hq + h * p.G + gq : -1;
+      my_mask[6 * BM] = (c * p.Hq + h * p.G + gq) * p.NQ + qoff + tok;
     }
-    const int inv_a = ns0 + min(tok, g.T - 1) + 1, inv_b = ns0 + g.T;   // rows this query may not see
     const float sl = p.scale_log2;
     float m_used = -INFINITY, l = 0.f;
     bool ok = true;
@@ -435,7 +527,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
         const uint32_t off_a = (ea / 64) * L::HALF_Q, off_b = (eb / 64) * L::HALF_Q;
         const int ca = (ea % 64) / 8, cb = (eb % 64) / 8;
         const float4* rope4 = reinterpret_cast<const float4*>(p.rope);
-        const int pos_base = g.P + vq * FT + (g.F - 1) * g.T;
+
 #pragma unroll
         for (int b4 = 0; b4 < NCH; b4 += 4) {
           uint4 xa[4], xb[4];
@@ -444,12 +536,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             const int rr = rr0 + b4 + q, qi = rr >> 7, r = rr & 127;
-            const int qtok = min(t0 + qi * p.TQ + r / p.G, g.T - 1);
+            const int qtok = min(t0 + qi * p.TQ + r / p.G, n_seg - 1);
             rp[q] = smem + L::Q_OFF + qi * L::QT;
             xa[q] = *reinterpret_cast<const uint4*>(rp[q] + off_a + tc::sw128_off(r, ca));
             xb[q] = *reinterpret_cast<const uint4*>(rp[q] + off_b + tc::sw128_off(r, cb));
 #pragma unroll
-            for (int w4 = 0; w4 < 4; ++w4) cs[q][w4] = __ldg(rope4 + ((size_t)(pos_base + qtok) * HALF + ea) / 2 + w4);
+            for (int w4 = 0; w4 < 4; ++w4) cs[q][w4] = __ldg(rope4 + ((size_t)(pos0 + qtok) * HALF + ea) / 2 + w4);
           }
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
@@ -476,14 +568,23 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
       for (int cb = 0; cb < BN / 32; ++cb)
         tc::tmem_ld32(tS + cb * 32, *reinterpret_cast<uint32_t(*)[32]>(v + cb * 32));
       const int r0 = s_tiles[j];
-      const int a = inv_a - r0, b = inv_b - r0, e = row_end - r0;
-      const bool full = (a >= BN || b <= 0 || a >= b) && e >= BN;
+      const int a = a1 - r0, e = row_end - r0;
+      const bool full = (n1 == 0 || a >= BN || a + n1 <= 0) && e >= BN;
       tc::tmem_wait_ld();
       if (!__all_sync(0xffffffffu, full)) {
-        const uint32_t span = (uint32_t)max(b - a, 0);
 #pragma unroll
         for (int k = 0; k < BN; ++k)
-          if (!((uint32_t)(k - a) >= span && k < e)) v[k] = __float_as_uint(-INFINITY);
+          if (!((uint32_t)(k - a) >= (uint32_t)n1 && k < e)) v[k] = __float_as_uint(-INFINITY);
+      }
+      if (wrap) {
+        // the second run of a hole that wraps around the end of the ring
+        const int b2 = tc::ld_shared_s32(mask_sa) - r0;
+        const uint32_t n2 = (uint32_t)tc::ld_shared_s32(mask_sa + 2 * BM * 4);
+        if (!__all_sync(0xffffffffu, n2 == 0 || b2 >= BN || b2 + (int)n2 <= 0)) {
+#pragma unroll
+          for (int k = 0; k < BN; ++k)
+            if ((uint32_t)(k - b2) < n2) v[k] = __float_as_uint(-INFINITY);
+        }
       }
       // row max: four chains of three-input maxima
       float m4[4];
@@ -553,14 +654,14 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
     if (done) {
       tc::tc_fence_after();
       const float inv_l = 1.f / l;
-      const size_t tok_row = (size_t)c * (g.V * g.T) + vq * g.T + tok;
-      uint16_t* orow = p.out + (tok_row * p.Hq + h * p.G + gq) * D;
+      const int o_row = my_mask[4 * BM];
+      uint16_t* orow = p.out + (size_t)max(o_row, 0) * D;
 #pragma unroll 1
       for (int cb = 0; cb < D / 32; ++cb) {
         uint32_t o[32];
         tc::tmem_ld32(tO + cb * 32, o);
         tc::tmem_wait_ld();
-        if (valid) {
+        if (o_row >= 0) {
           uint4 pk[4];
           uint32_t* pw = reinterpret_cast<uint32_t*>(pk);
 #pragma unroll
@@ -571,8 +672,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
           for (int k = 0; k < 4; ++k) dst[k] = pk[k];
         }
       }
-      if (valid && p.lse)
-        p.lse[((size_t)c * p.Hq + h * p.G + gq) * (g.V * g.T) + vq * g.T + tok] =
+      if (o_row >= 0 && p.lse)
+        p.lse[my_mask[6 * BM]] =
             (m_used + __log2f(l)) * 0.69314718055994531f;
     } else if (nt > 0 && *s_abort) {
       set_status(p.status, SKV_DEV_TIMEOUT);
@@ -649,18 +750,20 @@ cudaError_t make_kv_tmaps(const Geom& g, const void* k, const void* vt, int k_bo
   return cudaSuccess;
 }
 
-cudaError_t launch_prefill_tc(const Geom& g, int Hq, const void* q, void* out, float* lse, const void* k,
-                              const void* vt, const float* rope, const int32_t* head, float sm_scale,
-                              int32_t* status, uint64_t wait_ns, cudaStream_t st) {
+cudaError_t launch_prefill_tc(const Geom& g, int Hq, const PrefillQuery& qs, const void* q, void* out, float* lse,
+                              const void* k, const void* vt, const float* rope, const int32_t* head,
+                              float sm_scale, int32_t* status, uint64_t wait_ns, cudaStream_t st) {
   if ((g.row_cap + BN - 1) / BN > MAX_TILES || g.V > MAX_VIEWS) return cudaErrorNotSupported;
+  // output rows (token, head) and LSE entries are indexed in 32 bits
+  if ((long long)g.C * qs.NQ * Hq > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
   CUtensorMap tk, tv, tq;
   cudaError_t e = make_kv_tmaps(g, k, vt, HN, g.d / 2, &tk, &tv);
   if (e != cudaSuccess) return e;
   {
-    // queries [C * V * T tokens][Hq][d] bf16: a box is 64 columns of the G
+    // queries [C * NQ tokens][Hq][d] bf16: a box is 64 columns of the G
     // heads of one kv head for TQ tokens, i.e. 128 rows (token, head) of 128 B
     const int G = Hq / g.Hkv;
-    cuuint64_t dims[3] = {(cuuint64_t)g.d, (cuuint64_t)Hq, (cuuint64_t)g.C * g.V * g.T};
+    cuuint64_t dims[3] = {(cuuint64_t)g.d, (cuuint64_t)Hq, (cuuint64_t)g.C * qs.NQ};
     cuuint64_t strides[2] = {(cuuint64_t)g.d * 2, (cuuint64_t)Hq * g.d * 2};
     cuuint32_t box[3] = {64, (cuuint32_t)G, (cuuint32_t)(BM / G)};
     cuuint32_t es[3] = {1, 1, 1};
@@ -676,7 +779,17 @@ cudaError_t launch_prefill_tc(const Geom& g, int Hq, const void* q, void* out, f
   p.Hq = Hq;
   p.G = Hq / g.Hkv;
   p.TQ = BM / p.G;
-  p.pairs = (g.T + 4 * p.TQ - 1) / (4 * p.TQ);
+  const int blk_tok = 4 * p.TQ;                    // tokens of one CTA pair
+  p.n_tail = qs.n_tail;
+  p.nbt = (qs.n_tail + blk_tok - 1) / blk_tok;
+  p.nf = qs.nf;
+  p.nbf = (g.T + blk_tok - 1) / blk_tok;
+  p.nbp = qs.prefix ? (g.P + blk_tok - 1) / blk_tok : 0;
+  p.items = p.nbt + g.V * p.nf * p.nbf + p.nbp;
+  p.NQ = qs.NQ;
+  p.q_view0 = qs.q_view0;
+  p.q_tail0 = qs.q_tail0;
+  p.tail_len = qs.tail_len;
   p.q = static_cast<const uint16_t*>(q);
   p.out = static_cast<uint16_t*>(out);
   p.lse = lse;
@@ -685,7 +798,8 @@ cudaError_t launch_prefill_tc(const Geom& g, int Hq, const void* q, void* out, f
   p.status = status;
   p.scale_log2 = sm_scale * 1.4426950408889634f;
   p.wait_ns = wait_ns ? wait_ns : 2000000000ull;
-  const long long blocks = 2LL * g.C * g.Hkv * g.V * p.pairs;
+  if (p.nbt > 0 && !qs.tail_len) return cudaErrorInvalidValue;
+  const long long blocks = 2LL * g.C * g.Hkv * p.items;
   if (blocks <= 0) return cudaSuccess;
   if (blocks > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
   const bool sw = p.wait_ns < tc::kSuspendHintNs;

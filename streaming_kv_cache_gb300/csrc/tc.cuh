@@ -9,6 +9,13 @@
 namespace skv {
 namespace tc {
 
+// 32-bit load from a shared-memory address (shared window offset)
+__device__ __forceinline__ int ld_shared_s32(uint32_t addr) {
+  int v;
+  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
@@ -70,54 +77,44 @@ __device__ __forceinline__ bool mbar_try_wait_short(uint32_t bar, uint32_t parit
 // Poll try(bar, parity) until it succeeds.  The wait is bounded: after
 // limit_ns nanoseconds (counted in SM cycles at the 2.07 GHz maximum clock,
 // so a slower clock only lengthens it) it raises *abort and returns false; it
-// also returns false once another thread has raised *abort.  A suspended
-// try_wait may sleep up to the suspend hint, and the clock is read every 64
-// polls, so a limit far under the hint is not kept; kernels compiled with
-// SHORT (chosen by the host for such limits) poll without suspending and read
-// the clock at every poll instead.
-template <bool SHORT, typename Try>
+// also returns false once another thread has raised *abort.  The clock is
+// read every 64 polls, or at every poll with EVERY.
+template <bool EVERY, typename Try>
 __device__ __forceinline__ bool bounded_wait(Try try_fn, uint32_t bar, uint32_t parity, uint64_t limit_ns,
                                              volatile int* abort) {
-  if constexpr (SHORT) {
-    const long long limit = (long long)(limit_ns * 2.07);
-    const long long t0 = clock64();
-    for (;;) {
-      if (mbar_try_wait_short(bar, parity)) return true;
+  if (try_fn(bar, parity)) return true;
+  const long long limit = (long long)(limit_ns * 2.07);
+  const long long t0 = clock64();
+  for (uint32_t it = 1;; ++it) {
+    if (try_fn(bar, parity)) return true;
+    if (EVERY || (it & 63) == 0) {
+      if (*abort) return false;
       if (clock64() - t0 > limit) {
         *abort = 1;
         return false;
-      }
-      if (*abort) return false;
-    }
-  } else {
-    if (try_fn(bar, parity)) return true;
-    const long long limit = (long long)(limit_ns * 2.07);
-    const long long t0 = clock64();
-    for (uint32_t it = 1;; ++it) {
-      if (try_fn(bar, parity)) return true;
-      if ((it & 63) == 0) {
-        if (*abort) return false;
-        if (clock64() - t0 > limit) {
-          *abort = 1;
-          return false;
-        }
       }
     }
   }
 }
 
-// Wait for the phase with the given parity to complete (bounded, see bounded_wait).
-template <bool SHORT = false>
+// Wait for the phase with the given parity to complete (bounded, see
+// bounded_wait).  A suspended try_wait may sleep up to the suspend hint, so a
+// limit far under the hint is not kept: kernels compiled with SW (chosen by
+// the host for such limits) poll without suspending and read the clock at
+// every poll instead.
+template <bool SW = false>
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns,
                                           volatile int* abort) {
-  return bounded_wait<SHORT>(mbar_try_wait, bar, parity, limit_ns, abort);
+  if constexpr (SW) return bounded_wait<true>(mbar_try_wait_short, bar, parity, limit_ns, abort);
+  else return bounded_wait<false>(mbar_try_wait, bar, parity, limit_ns, abort);
 }
 
-// The same with short polls, for the MMA issuer.
-template <bool SHORT = false>
+// The same with short polls (no suspend hint), for waiters on the critical
+// path.
+template <bool SW = false>
 __device__ __forceinline__ bool mbar_wait_short(uint32_t bar, uint32_t parity, uint64_t limit_ns,
                                                 volatile int* abort) {
-  return bounded_wait<SHORT>(mbar_try_wait_short, bar, parity, limit_ns, abort);
+  return bounded_wait<SW>(mbar_try_wait_short, bar, parity, limit_ns, abort);
 }
 
 // A value the compiler must (re)compute where it stands: keeps loop-invariant
@@ -195,12 +192,31 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
   return ok != 0;
 }
 
+__device__ __forceinline__ bool mbar_try_wait_cluster_short(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Bounded wait (as mbar_wait) with cluster-scope acquire: for barriers that
 // receive arrivals from the peer CTA or from a pair MMA's commit.
-template <bool SHORT = false>
+template <bool SW = false>
 __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, uint64_t limit_ns,
                                                   volatile int* abort) {
-  return bounded_wait<SHORT>(mbar_try_wait_cluster, bar, parity, limit_ns, abort);
+  if constexpr (SW) return bounded_wait<true>(mbar_try_wait_cluster_short, bar, parity, limit_ns, abort);
+  else return bounded_wait<false>(mbar_try_wait_cluster, bar, parity, limit_ns, abort);
+}
+
+// The same with short polls.
+template <bool SW = false>
+__device__ __forceinline__ bool mbar_wait_cluster_short(uint32_t bar, uint32_t parity, uint64_t limit_ns,
+                                                        volatile int* abort) {
+  return bounded_wait<SW>(mbar_try_wait_cluster_short, bar, parity, limit_ns, abort);
 }
 
 __device__ __forceinline__ void cluster_sync() {

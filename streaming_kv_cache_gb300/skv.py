@@ -21,7 +21,7 @@ SKV_DEV_TIMEOUT, SKV_DEV_BAD_HEAD, SKV_DEV_TAIL_OVERFLOW, SKV_DEV_BAD_TAIL = 1, 
 # every function the C header declares
 EXPORTS = ("skv_version", "skv_status_string", "skv_last_cuda_error", "skv_row_cap",
            "skv_build_rope_table", "kv_write_rows", "kv_stream_insert", "kv_stream_insert_noalloc",
-           "stream_attn_prefill",
+           "stream_attn_prefill", "stream_attn_prefill_tail", "stream_attn_window",
            "skv_verify_workspace_bytes", "stream_attn_verify")
 
 
@@ -69,6 +69,9 @@ def lib():
             "kv_stream_insert": ([cp, P, P, P], ctypes.c_int),
             "kv_stream_insert_noalloc": ([cp, P, P, P], ctypes.c_int),
             "stream_attn_prefill": ([cp, I32, P, P, P, ctypes.c_float, P], ctypes.c_int),
+            "stream_attn_prefill_tail": ([cp, I32, I32, P, P, P, P, P, P, ctypes.c_float, P],
+                                         ctypes.c_int),
+            "stream_attn_window": ([cp, I32, P, P, P, ctypes.c_float, P], ctypes.c_int),
             "skv_verify_workspace_bytes": ([cp, I32, I32], SZ),
             "stream_attn_verify": ([cp, I32, I32, P, P, P, P, P, P, P, P, P, P, SZ,
                                     ctypes.c_float, P], ctypes.c_int),
@@ -215,6 +218,54 @@ def stream_attn_prefill(cache: StreamCache, q_new: torch.Tensor, sm_scale: float
     dd = cache.desc()
     _check(lib().stream_attn_prefill(ctypes.byref(dd), Hq, _ptr(q_new), _ptr(out), _ptr(lse),
                                      float(sm_scale), _stream()), "stream_attn_prefill")
+    return (out, lse) if lse is not None else out
+
+
+def _lse_arg(lse, C, Hq, n, device):
+    if lse is True:
+        lse = torch.empty((C, Hq, n), dtype=torch.float32, device=device)
+    if isinstance(lse, torch.Tensor):
+        _need(lse, (C, Hq, n), torch.float32, "lse")
+        return lse
+    return None
+
+
+def stream_attn_prefill_tail(cache: StreamCache, tail_len: torch.Tensor, q_tail: torch.Tensor,
+                             k_tail: torch.Tensor, v_tail: torch.Tensor, sm_scale: float,
+                             out: torch.Tensor | None = None,
+                             lse: torch.Tensor | bool | None = None):
+    """Writes the tokens' K/V after tail_len[c] tail rows and returns their
+    attention output (and lse when asked for).  The caller advances
+    tail_len by the number of tokens."""
+    C, n, Hq, d = q_tail.shape
+    _need(q_tail, (cache.C, n, Hq, cache.d), torch.bfloat16, "q_tail")
+    _need(k_tail, (cache.C, n, cache.Hkv, cache.d), torch.bfloat16, "k_tail")
+    _need(v_tail, (cache.C, n, cache.Hkv, cache.d), torch.bfloat16, "v_tail")
+    _need(tail_len, (cache.C,), torch.int32, "tail_len")
+    if out is None:
+        out = torch.empty_like(q_tail)
+    _need(out, q_tail.shape, torch.bfloat16, "out")
+    lse = _lse_arg(lse, C, Hq, n, q_tail.device)
+    dd = cache.desc()
+    _check(lib().stream_attn_prefill_tail(ctypes.byref(dd), Hq, n, _ptr(tail_len), _ptr(q_tail),
+                                          _ptr(k_tail), _ptr(v_tail), _ptr(out), _ptr(lse),
+                                          float(sm_scale), _stream()), "stream_attn_prefill_tail")
+    return (out, lse) if lse is not None else out
+
+
+def stream_attn_window(cache: StreamCache, q_win: torch.Tensor, sm_scale: float,
+                       out: torch.Tensor | None = None, lse: torch.Tensor | bool | None = None):
+    """Every window token as a query (logical order: prefix, then each view's
+    frames oldest to newest).  Returns out (and lse when asked for)."""
+    C, n, Hq, d = q_win.shape
+    _need(q_win, (cache.C, cache.n_visual, Hq, cache.d), torch.bfloat16, "q_win")
+    if out is None:
+        out = torch.empty_like(q_win)
+    _need(out, q_win.shape, torch.bfloat16, "out")
+    lse = _lse_arg(lse, C, Hq, n, q_win.device)
+    dd = cache.desc()
+    _check(lib().stream_attn_window(ctypes.byref(dd), Hq, _ptr(q_win), _ptr(out), _ptr(lse),
+                                    float(sm_scale), _stream()), "stream_attn_window")
     return (out, lse) if lse is not None else out
 
 

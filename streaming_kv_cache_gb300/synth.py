@@ -115,6 +115,7 @@ def normal_bf16(shape, *seed_parts, scale: float = 1.0) -> np.ndarray:
 #   frame K/V  [C][V][T][Hkv][d]     new-frame Q  [C][V*T][Hq][d]
 #   prefix K/V [C][P][Hkv][d]        tail K/V     [C][n][Hkv][d]
 #   verify block Q [C][blk][Hq][d], K/V [C][blk][Hkv][d]
+#   window Q [C][P+V*F*T][Hq][d]    tail-token Q [C][n][Hq][d], K/V [C][n][Hkv][d]
 
 def prefix_kv(w: Workload, tag: str = ""):
     shp = (w.C, w.P, w.Hkv, w.d)
@@ -137,6 +138,19 @@ def frame_q(w: Workload, insert_index: int, tag: str = ""):
 def tail_kv(w: Workload, n: int, tag: str = ""):
     shp = (w.C, n, w.Hkv, w.d)
     return (normal_bf16(shp, w.name, tag, "tail_k"), normal_bf16(shp, w.name, tag, "tail_v"))
+
+
+def window_q(w: Workload, tag: str = ""):
+    """Queries of every window token, logical order: [C][P + V*F*T][Hq][d]."""
+    return normal_bf16((w.C, w.n_window, w.Hq, w.d), w.name, tag, "window_q", scale=w.q_scale)
+
+
+def tail_block(w: Workload, n: int, tag: str = ""):
+    """Q, K, V of n tokens that follow the views (trajectory / text)."""
+    q = normal_bf16((w.C, n, w.Hq, w.d), w.name, tag, n, "tail_q", scale=w.q_scale)
+    k = normal_bf16((w.C, n, w.Hkv, w.d), w.name, tag, n, "tail_blk_k")
+    v = normal_bf16((w.C, n, w.Hkv, w.d), w.name, tag, n, "tail_blk_v")
+    return q, k, v
 
 
 def verify_block(w: Workload, tag: str = ""):

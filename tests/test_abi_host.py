@@ -108,6 +108,30 @@ def test_call_arguments_are_checked(L):
     assert L.stream_attn_verify(r, 32, 0, *args, None, None, None, None, p(FAKE), ws, 1.0, None) == skv.SKV_ERR_INVALID
 
 
+def test_tail_and_window_arguments(L):
+    d = _desc()
+    p = ctypes.c_void_p
+    r = ctypes.byref(d)
+    t = [p(FAKE)] * 4            # tail_len, q, k, v
+    # token count outside [1, tail_cap]; group size; scale; misaligned tensors / lse
+    assert L.stream_attn_prefill_tail(r, 32, 0, *t, p(FAKE), None, 1.0, None) == skv.SKV_ERR_INVALID
+    assert L.stream_attn_prefill_tail(r, 32, 129, *t, p(FAKE), None, 1.0, None) == skv.SKV_ERR_INVALID
+    assert L.stream_attn_prefill_tail(r, 30, 9, *t, p(FAKE), None, 1.0, None) == skv.SKV_ERR_INVALID
+    assert L.stream_attn_prefill_tail(r, 24, 9, *t, p(FAKE), None, 1.0, None) == skv.SKV_ERR_UNSUPPORTED
+    assert L.stream_attn_prefill_tail(r, 32, 9, *t, p(FAKE), None, -1.0, None) == skv.SKV_ERR_INVALID
+    assert L.stream_attn_prefill_tail(r, 32, 9, *t[:3], p(FAKE + 8), p(FAKE), None, 1.0, None) == skv.SKV_ERR_INVALID
+    assert L.stream_attn_prefill_tail(r, 32, 9, None, *t[1:], p(FAKE), None, 1.0, None) == skv.SKV_ERR_INVALID
+    assert L.stream_attn_prefill_tail(r, 32, 9, *t, p(FAKE), p(FAKE + 2), 1.0, None) == skv.SKV_ERR_INVALID
+    assert L.stream_attn_window(r, 30, p(FAKE), p(FAKE), None, 1.0, None) == skv.SKV_ERR_INVALID
+    assert L.stream_attn_window(r, 24, p(FAKE), p(FAKE), None, 1.0, None) == skv.SKV_ERR_UNSUPPORTED
+    assert L.stream_attn_window(r, 32, p(FAKE + 8), p(FAKE), None, 1.0, None) == skv.SKV_ERR_INVALID
+    assert L.stream_attn_window(r, 32, p(FAKE), None, None, 1.0, None) == skv.SKV_ERR_INVALID
+    assert L.stream_attn_window(r, 32, p(FAKE), p(FAKE), None, float("nan"), None) == skv.SKV_ERR_INVALID
+    bad = _desc(head_dim=96)
+    assert L.stream_attn_window(ctypes.byref(bad), 32, p(FAKE), p(FAKE), None, 1.0, None) == skv.SKV_ERR_INVALID
+    assert L.stream_attn_prefill_tail(ctypes.byref(bad), 32, 9, *t, p(FAKE), None, 1.0, None) == skv.SKV_ERR_INVALID
+
+
 def test_rope_table_arguments(L):
     p = ctypes.c_void_p
     assert L.skv_build_rope_table(None, 10, 128, 1e4, None) == skv.SKV_ERR_INVALID
