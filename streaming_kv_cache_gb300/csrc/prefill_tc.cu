@@ -57,7 +57,7 @@ namespace {
 constexpr int BM = 128;          // rows per query tile (per CTA)
 constexpr int BN = 128;          // keys per tile (pair)
 constexpr int HN = BN / 2;       // keys per tile loaded by one CTA
-constexpr int NST = 4;           // K and V stages
+constexpr int NST = 3;           // K and V stages (three ran faster than four: a smaller carve-out, more L1)
 constexpr int NTHREADS = 512;
 constexpr int WARP_KTMA = 8, WARP_MMA = 9, WARP_VFWD = 10, WARP_VTMA = 11, WARP_ROPE = 12;
 // register split (launch: 512 threads x 128): 2 x 128 x 176 + 128 x 56 + 128 x 104 = 65536
@@ -690,7 +690,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
   }
 }
 
-// Raise the kernel's dynamic shared-memory limit once per device.
+// Raise the kernel's dynamic shared-memory limit once per device, and ask
+// for the smallest shared-memory carve-out that holds it: the rest of the
+// SM's 256 KB stays L1, which serves the rotary-table loads (measured: the
+// largest carve-out made the 36-layer call 3% slower).
 template <typename K>
 cudaError_t set_smem_once(K kernel, int bytes, int variant) {
   static int done[64][4];
@@ -699,6 +702,8 @@ cudaError_t set_smem_once(K kernel, int bytes, int variant) {
   if (e != cudaSuccess) return e;
   if (dev >= 0 && dev < 64 && done[dev][variant]) return cudaSuccess;
   e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxL1);
   if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev][variant] = 1;
   return e;
 }
