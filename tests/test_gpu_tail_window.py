@@ -199,3 +199,39 @@ def test_window_and_tail_degenerate_geometries(geo):
     _window_check(pair, "a")
     tail = _set_tails(pair, [3, 0])
     _tail_check(pair, tail, 45, "b")
+
+
+def test_streams_at_different_phases_in_one_launch():
+    """Several independent streams (vehicles) in one launch of each call:
+    every cache's ring has turned a different number of times (its own head)
+    and its tail holds a different number of tokens.  Insert, prefill of the
+    new frames, the whole window, tail tokens and a verify block are each one
+    launch over all caches and match the oracle cache by cache."""
+    w = W["alpamayo_step"].with_(C=4, blk=9)
+    pair = Pair(w, "phase")
+    pair.fill()
+    heads = [(3 * c) % w.F for c in range(w.C)]
+    pair.cache.head.copy_(torch.tensor(heads, dtype=torch.int32)[:, None].expand(w.C, w.V).contiguous().cuda())
+    for c, win in pair.win.items():
+        for dq in win.views:
+            dq.rotate(-heads[c])     # logical frame f now lives in slot (head + f) mod F
+    pair.insert()
+    got_heads = pair.cache.head.cpu().numpy()
+    np.testing.assert_array_equal(got_heads[:, 0], [(h + 1) % w.F for h in heads])
+    q = synth.frame_q(w, pair.n_inserts - 1, "phase")
+    got = bf16_dev_to_f64(skv.stream_attn_prefill(pair.cache, to_dev(q), w.sm_scale))
+    for c, win in pair.win.items():
+        want, _ = O.stream_prefill(win, q[c], w.theta, w.sm_scale)
+        assert_close(got[c], want, "prefill, stream %d (head %d)" % (c, heads[c]))
+    rows = np.array([0, 255, 256, w.P + 5, w.P + w.T + 3, w.n_window // 2, w.n_window - 1])
+    _window_check(pair, "w", rows=rows)
+    tail = _set_tails(pair, [0, 7, 30, 64])
+    _tail_check(pair, tail, 12, "t")
+    tail += 12
+    bq, bk, bv = synth.verify_block(w, "phase")
+    out, _, _ = skv.stream_attn_verify(pair.cache, tail, to_dev(bq), to_dev(bk), to_dev(bv), w.sm_scale)
+    got = bf16_dev_to_f64(out)
+    for c, win in pair.win.items():
+        want, _ = O.stream_verify(win, bq[c], bk[c], bv[c], w.theta, w.sm_scale)
+        assert_close(got[c], want, "verify, stream %d" % c)
+    assert pair.cache.device_status() == 0
