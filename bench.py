@@ -124,7 +124,8 @@ def source_sha(kernel_file: str) -> str:
 
 class ClockSampler:
     """nvidia-smi every 50 ms around the timed region; summary() keeps the
-    samples whose timestamps fall between mark_start() and mark_stop()."""
+    samples whose timestamps fall between mark_start() and mark_stop()
+    (the board's power reading is a trailing average, so it is not kept)."""
     FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -162,7 +163,7 @@ class ClockSampler:
             self.lines = [l for l in out.splitlines() if l.strip()]
 
     def summary(self):
-        sm, mx, reasons, power = [], 0.0, set(), []
+        sm, mx, reasons = [], 0.0, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in self.lines:
             f = [x.strip() for x in line.split(",")]
@@ -174,15 +175,13 @@ class ClockSampler:
                     continue
                 sm.append(float(f[2]))
                 mx = max(mx, float(f[3]))
-                power.append(float(f[4]))
             except ValueError:
                 continue
             for n, val in zip(names, f[6:10]):
                 if val.lower().startswith("active"):
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx or None,
-                "reasons": sorted(reasons), "samples": len(sm),
-                "power_w_median": statistics.median(power) if power else None}
+                "reasons": sorted(reasons), "samples": len(sm)}
 
 
 # ---------------------------------------------------------------------------

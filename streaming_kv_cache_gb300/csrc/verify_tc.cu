@@ -607,9 +607,10 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         }
         // scale-and-shift runs on packed fp32 pairs
         const uint64_t sl2 = f2_pack(sl, sl), nm2 = f2_pack(-m_used, -m_used);
-        float l8[8];
+        // the row sum in four packed fp32 pairs: one add per pair of probabilities
+        uint64_t l2[4];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) l8[q] = 0.f;
+        for (int q = 0; q < 4; ++q) l2[q] = 0ull;
 #pragma unroll
         for (int cb = 0; cb < BN / 32; ++cb) {
           uint32_t pk[16];
@@ -625,12 +626,17 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
               p0 = tc::ex2(x0);
               p1 = tc::ex2(x1);
             }
-            l8[(k >> 1) & 7] += p0 + p1;
+            l2[(k >> 1) & 3] = f2_add(l2[(k >> 1) & 3], f2_pack(p0, p1));
             pk[k >> 1] = pack_bf16x2(p0, p1);
           }
           tc::tmem_st16(tS + cb * 16, pk);
         }
-        l += ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
+        {
+          const uint64_t s2 = f2_add(f2_add(l2[0], l2[1]), f2_add(l2[2], l2[3]));
+          float s0, s1;
+          f2_unpack(s2, s0, s1);
+          l += s0 + s1;
+        }
         tc::tmem_wait_st();
         tc::tc_fence_before();
         __syncwarp();
