@@ -40,8 +40,9 @@
 //
 // TMEM (512 columns per CTA): S0 [0,128) S1 [128,256) O0 [256,256+D)
 // O1 [384,384+D); P_i (bf16 pairs) overwrites the first 64 columns of S_i.
-// Online softmax in the exp2 domain with lazy rescaling: O and l are only
-// rescaled when a row's running max grows by more than 8 (factor 256).
+// Online softmax in the exp2 domain with a lagging max: the row max is taken
+// on a query's first tile only, and O and l are rescaled only when a later
+// tile's probability sum passes 2^20.
 #include <cudaTypedefs.h>
 #include <math.h>
 
@@ -65,7 +66,7 @@ constexpr int REG_SOFTMAX = 176, REG_CTRL = 56, REG_ROPE = 104;
 static_assert(256 * REG_SOFTMAX + 128 * REG_CTRL + 128 * REG_ROPE == 65536, "register split");
 constexpr int MAX_TILES = 1024;
 constexpr int MAX_VIEWS = 64;
-constexpr float RESCALE_THRESHOLD = 8.0f;
+constexpr float LAG_LIMIT = 1048576.0f;   // 2^20: a tile's probability sum that triggers a rescale
 // pairs of every 16 in a 32-score chunk whose exponentials run on the FMA pipe
 constexpr int FMA_EXP_PAIRS = 0;
 constexpr uint64_t DRAIN_NS = 500000000ull;  // bounded wait for own in-flight copies/MMAs
@@ -586,22 +587,64 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
             if ((uint32_t)(k - b2) < n2) v[k] = __float_as_uint(-INFINITY);
         }
       }
-      // row max: four chains of three-input maxima
-      float m4[4];
+      // The row max is taken on a query's first tile only; later tiles keep
+      // the running max m_used.  A larger score then gives a probability above
+      // 1, which costs nothing while the tile's sum stays under LAG_LIMIT (bf16
+      // P and fp32 O and l keep their relative precision at any scale); a
+      // larger sum (or an infinite one) sends the warp through the rescale:
+      // the tile's own max, O and l scaled down to it, P again.
+      auto row_max = [&]() {
+        float m4[4];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) m4[q] = fmaxf(__uint_as_float(v[2 * q]), __uint_as_float(v[2 * q + 1]));
+        for (int q = 0; q < 4; ++q) m4[q] = fmaxf(__uint_as_float(v[2 * q]), __uint_as_float(v[2 * q + 1]));
 #pragma unroll
-      for (int k = 8; k < BN; k += 2)
-        m4[(k >> 1) & 3] = fmax3(m4[(k >> 1) & 3], __uint_as_float(v[k]), __uint_as_float(v[k + 1]));
-      float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-      mx *= sl;
-      const bool grow = j > 0 && mx > m_used + RESCALE_THRESHOLD;
+        for (int k = 8; k < BN; k += 2)
+          m4[(k >> 1) & 3] = fmax3(m4[(k >> 1) & 3], __uint_as_float(v[k]), __uint_as_float(v[k + 1]));
+        return fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * sl;
+      };
+      // P = 2^(s*scale - m) as bf16 pairs into the first 64 columns of S_i;
+      // scale-and-shift and the row sum run on packed fp32 pairs
+      auto p_pass = [&]() {
+        const uint64_t sl2 = f2_pack(sl, sl), nm2 = f2_pack(-m_used, -m_used);
+        uint64_t l2[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) l2[q] = 0ull;
+#pragma unroll
+        for (int cb = 0; cb < BN / 32; ++cb) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int k = 0; k < 32; k += 2) {
+            float x0, x1;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(v[cb * 32 + k]), __uint_as_float(v[cb * 32 + k + 1])), sl2, nm2),
+                      x0, x1);
+            float p0, p1;
+            if (fma_exp_pair(k >> 1, FMA_EXP_PAIRS)) {
+              exp2_fma_x2(x0, x1, p0, p1);
+            } else {
+              p0 = tc::ex2(x0);
+              p1 = tc::ex2(x1);
+            }
+            l2[(k >> 1) & 3] = f2_add(l2[(k >> 1) & 3], f2_pack(p0, p1));
+            pk[k >> 1] = pack_bf16x2(p0, p1);
+          }
+          tc::tmem_st16(tS + cb * 16, pk);
+        }
+        const uint64_t s2 = f2_add(f2_add(l2[0], l2[1]), f2_add(l2[2], l2[3]));
+        float s0, s1;
+        f2_unpack(s2, s0, s1);
+        return s0 + s1;
+      };
       if (j == 0) {
+        const float mx = row_max();
         m_used = (mx == -INFINITY) ? 0.f : mx;
-      } else if (__any_sync(0xffffffffu, grow)) {
+      }
+      float ts = p_pass();
+      if (__any_sync(0xffffffffu, !(ts <= LAG_LIMIT))) {
         // O_i holds tiles < j, all complete: S_i(j) was committed after PV_i(j-1).
-        // Rows whose max did not grow past the threshold keep theirs (alpha = 1).
-        const float m_new = grow ? mx : m_used;
+        // Rows whose max did not grow keep theirs (alpha = 1) and write the same P again.
+        tc::tmem_wait_st();
+        const float mx = row_max();
+        const float m_new = mx > m_used ? mx : m_used;
         const float alpha = tc::ex2(m_used - m_new);
         l *= alpha;
 #pragma unroll 1
@@ -613,42 +656,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
           for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
           tc::tmem_st32(tO + cb * 32, o);
         }
-        tc::tmem_wait_st();
         m_used = m_new;
+        ts = p_pass();
       }
-      // P = 2^(s*scale - m) as bf16 pairs into the first 64 columns of S_i
-      // scale-and-shift runs on packed fp32 pairs
-      const uint64_t sl2 = f2_pack(sl, sl), nm2 = f2_pack(-m_used, -m_used);
-      // the row sum in four packed fp32 pairs: one add per pair of probabilities
-      uint64_t l2[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) l2[q] = 0ull;
-#pragma unroll
-      for (int cb = 0; cb < BN / 32; ++cb) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int k = 0; k < 32; k += 2) {
-          float x0, x1;
-          f2_unpack(f2_fma(f2_pack(__uint_as_float(v[cb * 32 + k]), __uint_as_float(v[cb * 32 + k + 1])), sl2, nm2),
-                    x0, x1);
-          float p0, p1;
-          if (fma_exp_pair(k >> 1, FMA_EXP_PAIRS)) {
-            exp2_fma_x2(x0, x1, p0, p1);
-          } else {
-            p0 = tc::ex2(x0);
-            p1 = tc::ex2(x1);
-          }
-          l2[(k >> 1) & 3] = f2_add(l2[(k >> 1) & 3], f2_pack(p0, p1));
-          pk[k >> 1] = pack_bf16x2(p0, p1);
-        }
-        tc::tmem_st16(tS + cb * 16, pk);
-      }
-      {
-        const uint64_t s2 = f2_add(f2_add(l2[0], l2[1]), f2_add(l2[2], l2[3]));
-        float s0, s1;
-        f2_unpack(s2, s0, s1);
-        l += s0 + s1;
-      }
+      l += ts;
       tc::tmem_wait_st();
       tc::tc_fence_before();
       __syncwarp();
