@@ -224,6 +224,25 @@ def oracle_sample(seconds: float = 12.0):
 
 # ---------------------------------------------------------------------------
 
+def max_over_ranks(dist, values, device):
+    """The largest of each timing over all ranks (each rank's own values
+    when there is no process group): the job is as slow as its slowest
+    replica."""
+    if dist is None:
+        return [float(v) for v in values]
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def job_throughput(world: int, work_per_step: float, steps: int, ms: float, scale: float = 1e12) -> float:
+    """Whole-job throughput: every rank does work_per_step per step (weak
+    scaling), so the job does world * work_per_step * steps in ms (the
+    max over ranks)."""
+    return world * work_per_step * steps / (ms * 1e-3) / scale
+
+
 def emit(obj):
     print(json.dumps(obj), flush=True)
 
@@ -515,16 +534,12 @@ def main():
     torch.cuda.synchronize()
     e2e_ms = s2.elapsed_time(t2)
 
-    # max over ranks
-    if dist:
-        tt = torch.tensor([t_ms, e2e_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_ms, e2e_ms = float(tt[0]), float(tt[1])
+    t_ms, e2e_ms = max_over_ranks(dist, [t_ms, e2e_ms], dev)
 
     flop = prefill_flop(pw)
     ms_per_step = t_ms / args.steps
-    value = world * flop * args.steps / (t_ms * 1e-3) / 1e12
-    e2e_value = world * flop * args.steps / (e2e_ms * 1e-3) / 1e12
+    value = job_throughput(world, flop, args.steps, t_ms)
+    e2e_value = job_throughput(world, flop, args.steps, e2e_ms)
     pk, src = peaks()
     pre_tf = flop / (k_ms["prefill"] * 1e-3) / 1e12
     ver_gbs = verify_bytes(vw) / (k_ms["verify"] * 1e-3) / 1e9
