@@ -204,7 +204,7 @@ def oracle_sample(seconds: float = 12.0):
         return sum(4.0 * w.d * w.Hq * (win.new_frame_index(int(j) // w.T, int(j) % w.T) + 1)
                    for j in rows)
 
-    n, spent, done_flop, calls = 8, 0.0, 0.0, 0
+    n, spent, done_flop, calls, n_rows = 8, 0.0, 0.0, 0, 0
     rng = np.random.default_rng(0)
     while spent < seconds and calls < 64:
         rows = np.sort(rng.choice(w.n_new, size=min(n, w.n_new), replace=False))
@@ -214,12 +214,26 @@ def oracle_sample(seconds: float = 12.0):
         spent += dt
         done_flop += flop(rows)
         calls += 1
+        n_rows += len(rows)
         n = min(w.n_new, n * 2) if dt < seconds / 8 else n
-    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    affinity = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    cores = blas_threads() or affinity
     text = ("fp64 NumPy oracle, %d prefill calls on one layer cache of the scale-up workload "
-            "(%.0f query rows x 32 heads in total, full recompute over the 12,800-key window), "
-            "%.1f s" % (calls, done_flop / (4.0 * w.d * w.Hq * 7000), spent))
+            "(%d query rows x %d heads in total, full recompute over the %d-key window), "
+            "%.1f s, %d BLAS threads on %d host cores"
+            % (calls, n_rows, w.Hq, w.n_window, spent, cores, affinity))
     return done_flop / spent / 1e12, cores, text, spent
+
+
+def blas_threads():
+    """Threads of the BLAS NumPy calls into, where threadpoolctl can tell
+    (None otherwise)."""
+    try:
+        from threadpoolctl import threadpool_info
+    except ImportError:
+        return None
+    n = [i.get("num_threads", 0) for i in threadpool_info() if i.get("user_api") == "blas"]
+    return max(n) if n and max(n) > 0 else None
 
 
 # ---------------------------------------------------------------------------
