@@ -14,6 +14,11 @@ kernel's HBM GB/s and the insert's GB/s are reported beside it.  Inputs stay
 resident in HBM; the caches (about 2.8 GB) are far larger than L2, so
 consecutive steps cannot hit in L2.
 
+The end-to-end figure runs the same step from pinned host buffers: every
+step's inputs are copied up and its outputs copied down inside the timed
+region.  Step i+1's upload and step i's download run on two copy streams
+while step i's kernels run; the fully serial form is reported beside it.
+
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 """
 from __future__ import annotations
@@ -465,18 +470,25 @@ def main():
     launches_per_step = 1 + 1 + 2      # insert; prefill; verify: tail write (+ accept) and attention
     ev = {n: [] for n in ("insert", "prefill", "verify")}
 
-    def step(record):
+    # a step's device inputs and outputs (a second set serves the pipelined
+    # end-to-end loop below)
+    dev_in = [k_new, v_new, q_new, q_blk, k_blk, v_blk, tgt_d, drf_d]
+    dev_out = [p_out, v_out, acc, nxt]
+
+    def step(record, ins=dev_in, outs=dev_out):
+        kn, vn, qn, qb, kb, vb, tg, dr = ins
+        po, vo, ac, nx = outs
         if record:
             e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
             e[0].record()
-        skv.kv_stream_insert(pc, k_new, v_new)
+        skv.kv_stream_insert(pc, kn, vn)
         if record:
             e[1].record()
-        skv.stream_attn_prefill(pc, q_new, pw.sm_scale, out=p_out)
+        skv.stream_attn_prefill(pc, qn, pw.sm_scale, out=po)
         if record:
             e[2].record()
-        skv.stream_attn_verify(vc, tail0, q_blk, k_blk, v_blk, vw.sm_scale, target_ids=tgt_d,
-                               draft_ids=drf_d, ws=ws, out=v_out, accept_len=acc, next_token=nxt)
+        skv.stream_attn_verify(vc, tail0, qb, kb, vb, vw.sm_scale, target_ids=tg,
+                               draft_ids=dr, ws=ws, out=vo, accept_len=ac, next_token=nx)
         if record:
             e[3].record()
             ev["insert"].append((e[0], e[1]))
@@ -527,14 +539,13 @@ def main():
     d2h = sum(t.numel() * t.element_size() for t in outs)
 
     def e2e_step():
-        k_new.copy_(h_k, non_blocking=True); v_new.copy_(h_v, non_blocking=True)
-        q_new.copy_(h_q, non_blocking=True); q_blk.copy_(h_qb, non_blocking=True)
-        k_blk.copy_(h_kb, non_blocking=True); v_blk.copy_(h_vb, non_blocking=True)
-        tgt_d.copy_(h_t, non_blocking=True); drf_d.copy_(h_d, non_blocking=True)
+        for d, h in zip(dev_in, ins):
+            d.copy_(h, non_blocking=True)
         step(False)
-        h_out.copy_(p_out, non_blocking=True); h_vout.copy_(v_out, non_blocking=True)
-        h_acc.copy_(acc, non_blocking=True); h_nxt.copy_(nxt, non_blocking=True)
+        for h, d in zip(outs, dev_out):
+            h.copy_(d, non_blocking=True)
 
+    # serial form: copy in, compute, copy out, one after another on one stream
     for _ in range(args.warmup):
         e2e_step()
     torch.cuda.synchronize()
@@ -546,9 +557,66 @@ def main():
         e2e_step()
     t2.record()
     torch.cuda.synchronize()
-    e2e_ms = s2.elapsed_time(t2)
+    serial_ms = s2.elapsed_time(t2)
 
-    t_ms, e2e_ms = max_over_ranks(dist, [t_ms, e2e_ms], dev)
+    # pipelined form: step i+1's inputs go up on one copy stream and step i's
+    # outputs come down on another while step i's kernels run; device inputs
+    # and outputs are double-buffered so that no copy touches a buffer a
+    # kernel in flight still reads or writes.  Every step's copies stay inside
+    # the timed region.
+    dev_in2 = [dev_in, [torch.empty_like(t) for t in dev_in]]
+    dev_out2 = [dev_out, [torch.empty_like(t) for t in dev_out]]
+    up, down = torch.cuda.Stream(), torch.cuda.Stream()
+    ks = torch.cuda.current_stream()
+
+    def e2e_pipelined(n_steps):
+        in_ready = [torch.cuda.Event() for _ in range(2)]
+        used = [torch.cuda.Event() for _ in range(2)]      # the step that read set s is done
+        read = [torch.cuda.Event() for _ in range(2)]      # outputs of set s are on the host
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(ks)
+        up.wait_event(a)
+        down.wait_event(a)
+
+        def upload(k):
+            with torch.cuda.stream(up):
+                for d, h in zip(dev_in2[k], ins):
+                    d.copy_(h, non_blocking=True)
+                in_ready[k].record(up)
+
+        upload(0)
+        for i in range(n_steps):
+            k = i & 1
+            if i + 1 < n_steps:
+                if i >= 1:
+                    up.wait_event(used[k ^ 1])             # step i-1 read set k^1
+                upload(k ^ 1)
+            ks.wait_event(in_ready[k])
+            if i >= 2:
+                ks.wait_event(read[k])                      # step i-2's outputs are down
+            step(False, dev_in2[k], dev_out2[k])
+            used[k].record(ks)
+            down.wait_event(used[k])
+            with torch.cuda.stream(down):
+                for h, d in zip(outs, dev_out2[k]):
+                    h.copy_(d, non_blocking=True)
+                read[k].record(down)
+        ks.wait_event(read[(n_steps - 1) & 1])              # the copy-out stream is in order
+        b.record(ks)
+        return a, b
+
+    e2e_pipelined(args.warmup)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    s3, t3 = e2e_pipelined(args.steps)
+    torch.cuda.synchronize()
+    e2e_ms = s3.elapsed_time(t3)
+    status = pc.device_status() | vc.device_status()
+    if status:
+        raise RuntimeError("device status %d in the end-to-end loops: %s" % (status, skv.status_string(status)))
+
+    t_ms, e2e_ms, serial_ms = max_over_ranks(dist, [t_ms, e2e_ms, serial_ms], dev)
 
     flop = prefill_flop(pw)
     ms_per_step = t_ms / args.steps
@@ -593,7 +661,13 @@ def main():
                                 "frac": ins_gbs / pk["hbm_gbs"], "peak_source": tag},
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / args.steps},
+                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / args.steps,
+                    "copies": "pinned host buffers; step i+1's inputs up and step i's outputs "
+                              "down on two copy streams while step i's kernels run "
+                              "(double-buffered device inputs and outputs)",
+                    "serial": {"value": job_throughput(world, flop, args.steps, serial_ms),
+                               "ms_per_step": serial_ms / args.steps,
+                               "copies": "in, kernels, out one after another on one stream"}},
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clk.summary(),
         })
