@@ -262,6 +262,47 @@ def job_throughput(world: int, work_per_step: float, steps: int, ms: float, scal
     return world * work_per_step * steps / (ms * 1e-3) / scale
 
 
+def check_pipelined(torch, pipelined, step, dev_in, dev_out, h_in, h_out, heads):
+    """Untimed self-check of the overlapped end-to-end loop.  Four steps whose
+    host inputs alternate A B B A (the queries differ, so both double-buffer
+    slots change content between uses) run first one at a time on the
+    compute stream, then, from the same ring heads, through the overlapped
+    loop; every step's host outputs must be bit-identical.  (The prefill
+    streams keys in physical ring order, so its summation order follows the
+    ring heads; restoring them makes the two runs the same computation.)  A
+    copy that overtook the kernels using its buffer shows up as a mismatch.
+    Raises on a mismatch; returns a one-line description."""
+    q_b = list(h_in)
+    for j in (2, 3):                       # the prefill queries and the verify block queries
+        q_b[j] = (h_in[j].float() * -0.5).to(h_in[j].dtype).pin_memory()
+    variants = [h_in, q_b]
+    order = [0, 1, 1, 0]
+    saved = [t.clone() for t in heads]
+    want = []
+    for v in order:
+        for d, h in zip(dev_in, variants[v]):
+            d.copy_(h)
+        step(False)
+        torch.cuda.synchronize()
+        want.append([d.to("cpu", copy=True) for d in dev_out])
+    for t, c in zip(heads, saved):
+        t.copy_(c)
+    got = [[torch.empty_like(t).pin_memory() for t in h_out] for _ in order]
+    pipelined(len(order), host_in=lambda i: variants[order[i]], host_out=lambda i: got[i])
+    torch.cuda.synchronize()
+    for i in range(len(order)):
+        for name, a, b in zip(("prefill out", "verify out", "accept_len", "next_token"), got[i], want[i]):
+            if not torch.equal(a, b):
+                raise RuntimeError("overlapped end-to-end step %d: %s differs from the same step "
+                                   "run alone" % (i, name))
+    if torch.equal(want[0][0], want[1][0]):
+        raise RuntimeError("end-to-end self-check: the two input variants gave the same output")
+    for d, h in zip(dev_in, h_in):         # leave the timed inputs as they were
+        d.copy_(h)
+    return ("4 overlapped steps, inputs A B B A, from the same ring heads: host outputs "
+            "bit-identical to the same steps run one at a time")
+
+
 def emit(obj):
     print(json.dumps(obj), flush=True)
 
@@ -569,7 +610,7 @@ def main():
     up, down = torch.cuda.Stream(), torch.cuda.Stream()
     ks = torch.cuda.current_stream()
 
-    def e2e_pipelined(n_steps):
+    def e2e_pipelined(n_steps, host_in=lambda i: ins, host_out=lambda i: outs):
         in_ready = [torch.cuda.Event() for _ in range(2)]
         used = [torch.cuda.Event() for _ in range(2)]      # the step that read set s is done
         read = [torch.cuda.Event() for _ in range(2)]      # outputs of set s are on the host
@@ -578,19 +619,19 @@ def main():
         up.wait_event(a)
         down.wait_event(a)
 
-        def upload(k):
+        def upload(k, i):
             with torch.cuda.stream(up):
-                for d, h in zip(dev_in2[k], ins):
+                for d, h in zip(dev_in2[k], host_in(i)):
                     d.copy_(h, non_blocking=True)
                 in_ready[k].record(up)
 
-        upload(0)
+        upload(0, 0)
         for i in range(n_steps):
             k = i & 1
             if i + 1 < n_steps:
                 if i >= 1:
                     up.wait_event(used[k ^ 1])             # step i-1 read set k^1
-                upload(k ^ 1)
+                upload(k ^ 1, i + 1)
             ks.wait_event(in_ready[k])
             if i >= 2:
                 ks.wait_event(read[k])                      # step i-2's outputs are down
@@ -598,7 +639,7 @@ def main():
             used[k].record(ks)
             down.wait_event(used[k])
             with torch.cuda.stream(down):
-                for h, d in zip(outs, dev_out2[k]):
+                for h, d in zip(host_out(i), dev_out2[k]):
                     h.copy_(d, non_blocking=True)
                 read[k].record(down)
         ks.wait_event(read[(n_steps - 1) & 1])              # the copy-out stream is in order
@@ -615,6 +656,7 @@ def main():
     status = pc.device_status() | vc.device_status()
     if status:
         raise RuntimeError("device status %d in the end-to-end loops: %s" % (status, skv.status_string(status)))
+    e2e_check = check_pipelined(torch, e2e_pipelined, step, dev_in, dev_out, ins, outs, [pc.head, vc.head])
 
     t_ms, e2e_ms, serial_ms = max_over_ranks(dist, [t_ms, e2e_ms, serial_ms], dev)
 
@@ -665,6 +707,7 @@ def main():
                     "copies": "pinned host buffers; step i+1's inputs up and step i's outputs "
                               "down on two copy streams while step i's kernels run "
                               "(double-buffered device inputs and outputs)",
+                    "check": e2e_check,
                     "serial": {"value": job_throughput(world, flop, args.steps, serial_ms),
                                "ms_per_step": serial_ms / args.steps,
                                "copies": "in, kernels, out one after another on one stream"}},
