@@ -139,3 +139,24 @@ def test_rope_table_arguments(L):
     assert L.skv_build_rope_table(p(FAKE), 10, 127, 1e4, None) == skv.SKV_ERR_INVALID
     assert L.skv_build_rope_table(p(FAKE), 10, 128, -1.0, None) == skv.SKV_ERR_INVALID
     assert L.skv_build_rope_table(p(FAKE + 4), 10, 128, 1e4, None) == skv.SKV_ERR_INVALID
+
+
+def test_header_compiles_as_c_and_struct_layout_matches_the_binding(L, tmp_path):
+    """A C99 program built against the header and linked with the library:
+    the header is plain C, the no-GPU answers hold from C, and the size and
+    every field offset of skv_cache agree with the ctypes structure the
+    Python binding passes."""
+    exe = str(tmp_path / "abi_check")
+    src = os.path.join(os.path.dirname(os.path.abspath(__file__)), "abi_check.c")
+    lib_dir = os.path.dirname(B.LIB)
+    r = subprocess.run(["gcc", "-std=c99", "-Wall", "-Wextra", "-Werror", "-I",
+                        os.path.join(B.ROOT, "include"), src, "-L", lib_dir, "-lskv",
+                        "-Wl,-rpath," + lib_dir, "-o", exe], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([exe], capture_output=True, text=True)
+    assert r.returncode == 0, r.stdout + r.stderr
+    layout = dict(line.split() for line in r.stdout.splitlines() if not line.startswith("FAIL"))
+    assert int(layout["size"]) == ctypes.sizeof(skv.skv_cache)
+    for name, _ in skv.skv_cache._fields_:
+        assert int(layout[name]) == getattr(skv.skv_cache, name).offset, name
+    assert layout["fails"] == "0"
