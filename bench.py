@@ -303,6 +303,17 @@ def check_pipelined(torch, pipelined, step, dev_in, dev_out, h_in, h_out, heads)
             "bit-identical to the same steps run one at a time")
 
 
+def step_config() -> dict:
+    """The workload of one bench step, as both arms report it."""
+    return {"workload": "scaleup_36L step (insert + prefill, 36 layer caches, P=512, "
+                        "6 views x 8 frames x 256 tokens, 1536 queries, Hq=32/Hkv=8/d=128) "
+                        "+ alpamayo_verify (B=64, 9-token block, 16 tail tokens)",
+            "l2": "inputs larger than L2 (caches 2.8 GB), no flush",
+            "prefill_gflop_per_step": prefill_flop(PREFILL_W) / 1e9,
+            "verify_mb_per_step": verify_bytes(VERIFY_W) / 1e6,
+            "insert_mb_per_step": insert_bytes(PREFILL_W) / 1e6}
+
+
 def emit(obj):
     print(json.dumps(obj), flush=True)
 
@@ -324,7 +335,7 @@ def run_reference(args, rank, world):
           "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
           "ms_per_step": 1e3 * secs / max(1, args.steps), "higher_is_better": True,
           "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-          "config": {"workload": "scaleup_36L prefill sample on the host (oracle)"},
+          "config": step_config(),
           "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                            "sample": text},
           "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
@@ -681,13 +692,7 @@ def main():
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
-            "config": {"workload": "scaleup_36L step (insert + prefill, 36 layer caches, P=512, "
-                                   "6 views x 8 frames x 256 tokens, 1536 queries, Hq=32/Hkv=8/d=128) "
-                                   "+ alpamayo_verify (B=64, 9-token block, 16 tail tokens)",
-                       "l2": "inputs larger than L2 (caches 2.8 GB), no flush",
-                       "prefill_gflop_per_step": flop / 1e9,
-                       "verify_mb_per_step": verify_bytes(vw) / 1e6,
-                       "insert_mb_per_step": insert_bytes(pw) / 1e6},
+            "config": step_config(),
             "kernels_ms": k_ms,
             "roofline": {"bound": "tensor", "kernel": "stream_attn_prefill", "achieved": pre_tf,
                          "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
