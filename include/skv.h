@@ -197,7 +197,10 @@ int kv_stream_insert_noalloc(const skv_cache* cache, const void* k_new, const vo
  *        accumulation, rounded to nearest even once.
  * lse:   device fp32 [C][Hq][V*T] natural-log sum of exp of the scaled
  *        scores, or NULL.
- * Needs Hq % Hkv == 0 and 128 % (Hq/Hkv) == 0.
+ * Needs Hq % Hkv == 0 and 128 % (Hq/Hkv) == 0.  The kernel covers V <= 64,
+ * row_cap <= 131072 and C * (query tokens) * Hq < 2^31; outside that the
+ * call returns SKV_ERR_UNSUPPORTED and enqueues nothing (the same limits
+ * hold for stream_attn_prefill_tail and stream_attn_window).
  */
 int stream_attn_prefill(const skv_cache* cache, int32_t n_q_head, const void* q_new, void* out,
                         float* lse, float sm_scale, void* stream);
@@ -220,8 +223,9 @@ int stream_attn_prefill(const skv_cache* cache, int32_t n_q_head, const void* q_
  * q_tail:   device bf16 [C][n_tok][Hq][d]; k_tail, v_tail: [C][n_tok][Hkv][d].
  * out:      device bf16 [C][n_tok][Hq][d].
  * lse:      device fp32 [C][Hq][n_tok] or NULL.
- * Needs 1 <= n_tok <= tail_cap, Hq % Hkv == 0 and 128 % (Hq/Hkv) == 0.
- * tail_len[c] < 0 sets SKV_DEV_BAD_TAIL, tail_len[c] + n_tok > tail_cap sets
+ * Needs 1 <= n_tok <= tail_cap, Hq % Hkv == 0 and 128 % (Hq/Hkv) == 0, and
+ * the shape limits of stream_attn_prefill (checked before anything is
+ * written).  tail_len[c] < 0 sets SKV_DEV_BAD_TAIL, tail_len[c] + n_tok > tail_cap sets
  * SKV_DEV_TAIL_OVERFLOW; that cache is then neither written nor attended.
  */
 int stream_attn_prefill_tail(const skv_cache* cache, int32_t n_q_head, int32_t n_tok,
@@ -243,7 +247,8 @@ int stream_attn_prefill_tail(const skv_cache* cache, int32_t n_q_head, int32_t n
  * q_win: device bf16 [C][N][Hq][d], pre-RoPE, in logical order.
  * out:   device bf16 [C][N][Hq][d].
  * lse:   device fp32 [C][Hq][N] or NULL.
- * Needs Hq % Hkv == 0 and 128 % (Hq/Hkv) == 0.
+ * Needs Hq % Hkv == 0 and 128 % (Hq/Hkv) == 0, and the shape limits of
+ * stream_attn_prefill.
  */
 int stream_attn_window(const skv_cache* cache, int32_t n_q_head, const void* q_win, void* out,
                        float* lse, float sm_scale, void* stream);
@@ -275,10 +280,11 @@ size_t skv_verify_workspace_bytes(const skv_cache* cache, int32_t n_q_head, int3
  * ws: device workspace of ws_bytes >= skv_verify_workspace_bytes(); it must
  *     be zero-filled before its first use, the call leaves it ready for the
  *     next one (re-zero it after a call that set a device status bit).
- * Needs 1 <= blk <= tail_cap and Hq/Hkv <= 64; a block of more than 64 rows
- * per kv head (blk * Hq/Hkv) is taken 64 rows at a time, which needs Hq/Hkv to
- * divide 64.  tail_len + blk > tail_cap sets
- * SKV_DEV_TAIL_OVERFLOW and skips that cache.
+ * Needs 1 <= blk <= tail_cap, V <= 64 and Hq/Hkv <= 64 (else
+ * SKV_ERR_UNSUPPORTED); a block of more than 64 rows per kv head
+ * (blk * Hq/Hkv) is taken 64 rows at a time, which needs Hq/Hkv to divide
+ * 64.  tail_len + blk > tail_cap sets SKV_DEV_TAIL_OVERFLOW and skips that
+ * cache.
  */
 int stream_attn_verify(const skv_cache* cache, int32_t n_q_head, int32_t blk,
                        const int32_t* tail_len, const void* q_blk, const void* k_blk,

@@ -56,6 +56,22 @@ int check_cache(const skv_cache* c) {
   return SKV_OK;
 }
 
+// Shapes the tensor-core prefill kernel covers: its per-CTA tables hold the
+// ring heads of at most kMaxViews views and at most kPrefillMaxKeyTiles
+// 128-row key tiles per (cache, kv head), and output rows (token, head) are
+// indexed in 32 bits.  Checked here so that a call outside them enqueues
+// nothing (the tail prefill writes rows before it attends).
+constexpr int kMaxViews = 64;
+constexpr long long kPrefillMaxKeyTiles = 1024;
+constexpr long long kPrefillKeyTile = 128;
+
+int check_prefill_shape(const skv_cache* c, long long n_query, int n_q_head) {
+  if (c->n_view > kMaxViews) return SKV_ERR_UNSUPPORTED;
+  if ((c->row_cap + kPrefillKeyTile - 1) / kPrefillKeyTile > kPrefillMaxKeyTiles) return SKV_ERR_UNSUPPORTED;
+  if ((long long)c->n_cache * n_query * n_q_head > 0x7FFFFFFFLL) return SKV_ERR_UNSUPPORTED;
+  return SKV_OK;
+}
+
 }  // namespace
 
 namespace skv {
@@ -145,6 +161,7 @@ int stream_attn_prefill(const skv_cache* cache, int32_t n_q_head, const void* q_
   if (rc) return rc;
   if (n_q_head < 1 || n_q_head % cache->n_kv_head) return SKV_ERR_INVALID;
   if (128 % (n_q_head / cache->n_kv_head)) return SKV_ERR_UNSUPPORTED;
+  if ((rc = check_prefill_shape(cache, (long long)cache->n_view * cache->frame_len, n_q_head))) return rc;
   if (!(sm_scale > 0.f) || sm_scale != sm_scale) return SKV_ERR_INVALID;
   if (cache->n_cache == 0) return SKV_OK;
   if (!q_new || !out || !aligned16(q_new) || !aligned16(out)) return SKV_ERR_INVALID;
@@ -169,6 +186,7 @@ int stream_attn_prefill_tail(const skv_cache* cache, int32_t n_q_head, int32_t n
   if (n_q_head < 1 || n_q_head % cache->n_kv_head) return SKV_ERR_INVALID;
   if (n_tok < 1 || n_tok > cache->tail_cap) return SKV_ERR_INVALID;
   if (128 % (n_q_head / cache->n_kv_head)) return SKV_ERR_UNSUPPORTED;
+  if ((rc = check_prefill_shape(cache, n_tok, n_q_head))) return rc;
   if (!(sm_scale > 0.f) || sm_scale != sm_scale) return SKV_ERR_INVALID;
   if (cache->n_cache == 0) return SKV_OK;
   if (!tail_len || !q_tail || !k_tail || !v_tail || !out) return SKV_ERR_INVALID;
@@ -197,6 +215,10 @@ int stream_attn_window(const skv_cache* cache, int32_t n_q_head, const void* q_w
   if (rc) return rc;
   if (n_q_head < 1 || n_q_head % cache->n_kv_head) return SKV_ERR_INVALID;
   if (128 % (n_q_head / cache->n_kv_head)) return SKV_ERR_UNSUPPORTED;
+  if ((rc = check_prefill_shape(cache, (long long)cache->prefix_len +
+                                           (long long)cache->n_view * cache->n_frame * cache->frame_len,
+                                n_q_head)))
+    return rc;
   if (!(sm_scale > 0.f) || sm_scale != sm_scale) return SKV_ERR_INVALID;
   if (cache->n_cache == 0) return SKV_OK;
   if (!q_win || !out || !aligned16(q_win) || !aligned16(out)) return SKV_ERR_INVALID;
@@ -242,7 +264,7 @@ int stream_attn_verify(const skv_cache* cache, int32_t n_q_head, int32_t blk,
   if (ids && (!accept_len || !next_token)) return SKV_ERR_INVALID;
   const size_t ws_need = skv_verify_workspace_bytes(cache, n_q_head, blk);
   if (ws_bytes < ws_need || (ws_need && (!ws || !aligned16(ws)))) return SKV_ERR_INVALID;
-  if (cache->n_view > 64) return SKV_ERR_UNSUPPORTED;   // the verify kernel keeps <= 64 ring heads on chip
+  if (cache->n_view > kMaxViews) return SKV_ERR_UNSUPPORTED;   // the verify kernel keeps the ring heads on chip
   if ((rc = check_device())) return rc;
   const skv::Geom g = skv::geom_of(*cache);
   cudaStream_t st = (cudaStream_t)stream;

@@ -9,7 +9,7 @@ import subprocess
 import pytest
 
 from streaming_kv_cache_gb300 import build as B
-from streaming_kv_cache_gb300 import skv
+from streaming_kv_cache_gb300 import skv, synth
 
 HEADER = os.path.join(B.ROOT, "include", "skv.h")
 
@@ -160,3 +160,68 @@ def test_header_compiles_as_c_and_struct_layout_matches_the_binding(L, tmp_path)
     for name, _ in skv.skv_cache._fields_:
         assert int(layout[name]) == getattr(skv.skv_cache, name).offset, name
     assert layout["fails"] == "0"
+
+
+def _shape_desc(**kw):
+    """A descriptor with a consistent geometry (row_cap and rope_len derived)."""
+    g = dict(n_cache=2, n_view=4, n_frame=4, frame_len=180, prefix_len=256, tail_cap=128,
+             n_kv_head=8, head_dim=128)
+    g.update(kw)
+    need = g["prefix_len"] + g["n_view"] * g["n_frame"] * g["frame_len"] + g["tail_cap"]
+    return _desc(**g, row_cap=skv.skv_row_cap(g["prefix_len"], g["n_view"], g["n_frame"],
+                                              g["frame_len"], g["tail_cap"]), rope_len=need)
+
+
+def _prefill_family(L, d, Hq=32):
+    p = ctypes.c_void_p
+    r = ctypes.byref(d)
+    return (L.stream_attn_prefill(r, Hq, p(FAKE), p(FAKE), None, 1.0, None),
+            L.stream_attn_prefill_tail(r, Hq, 9, p(FAKE), p(FAKE), p(FAKE), p(FAKE), p(FAKE), None, 1.0,
+                                       None),
+            L.stream_attn_window(r, Hq, p(FAKE), p(FAKE), None, 1.0, None))
+
+
+def test_prefill_shape_limits_are_checked_before_anything_is_enqueued(L):
+    """Outside the kernel's tables (more than 64 views, more than 1024 key
+    tiles of 128 rows) the calls answer SKV_ERR_UNSUPPORTED on the host --
+    for the tail prefill before its rows are written -- while verify, which
+    has no tile table, only limits the views."""
+    assert _prefill_family(L, _shape_desc(n_view=65, n_frame=1, frame_len=1, prefix_len=0)) == \
+        (skv.SKV_ERR_UNSUPPORTED,) * 3
+    # the ring holds 4 x 4 x 180 = 2880 rows and the tail 128
+    big = _shape_desc(prefix_len=131072 - 2880 - 128 + 1, n_cache=1)    # 131,073 rows: 1025 tiles
+    assert (big.row_cap + 127) // 128 == 1025
+    assert _prefill_family(L, big) == (skv.SKV_ERR_UNSUPPORTED,) * 3
+    ok = _shape_desc(prefix_len=131072 - 2880 - 128, n_cache=0)         # 131,072 rows: 1024 tiles
+    assert (ok.row_cap + 127) // 128 == 1024
+    assert _prefill_family(L, ok) == (skv.SKV_OK,) * 3
+    p = ctypes.c_void_p
+    v65 = _shape_desc(n_view=65, n_frame=1, frame_len=1, prefix_len=0)
+    ws = L.skv_verify_workspace_bytes(ctypes.byref(v65), 32, 9)
+    assert L.stream_attn_verify(ctypes.byref(v65), 32, 9, *[p(FAKE)] * 5, None, None, None, None,
+                                p(FAKE), ws, 1.0, None) == skv.SKV_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("name", sorted(synth.WORKLOADS))
+def test_every_workload_geometry_is_within_the_kernels(L, name):
+    """The shape checks accept every workload's geometry (an empty cache set
+    returns SKV_OK once every shape check has passed)."""
+    w = synth.WORKLOADS[name]
+    d = _shape_desc(n_cache=0, n_view=w.V, n_frame=w.F, frame_len=w.T, prefix_len=w.P,
+                    tail_cap=w.tail_cap, n_kv_head=w.Hkv, head_dim=w.d)
+    assert _prefill_family(L, d, Hq=w.Hq) == (skv.SKV_OK,) * 3
+
+
+def test_host_shape_limits_match_the_kernels():
+    """The host-side limits in api.cu are the kernels' own table sizes."""
+    csrc = os.path.join(B.ROOT, "streaming_kv_cache_gb300", "csrc")
+
+    def const(fname, name):
+        src = open(os.path.join(csrc, fname)).read()
+        m = re.search(r"constexpr\s+(?:int|long long)\s+%s\s*=\s*(\d+)" % name, src)
+        assert m, (fname, name)
+        return int(m.group(1))
+
+    assert const("api.cu", "kMaxViews") == const("prefill_tc.cu", "MAX_VIEWS") == const("verify_tc.cu", "MAX_VIEWS")
+    assert const("api.cu", "kPrefillMaxKeyTiles") == const("prefill_tc.cu", "MAX_TILES")
+    assert const("api.cu", "kPrefillKeyTile") == const("prefill_tc.cu", "BN")
