@@ -23,8 +23,8 @@ def _built():
     build.build()
 
 
-# LSE bound: the tensor cores take the rotated Q and K rounded to bf16
-# (relative error 2^-9 each), so a score moves by about 2^-8 |q||k| sm_scale;
+# LSE bound: the tensor cores take the rotated Q and K rounded to fp16
+# (relative error 2^-11 each), so a score moves by about 2^-10 |q||k| sm_scale;
 # over N(0,1) inputs that stays well under 1e-2 in the log-sum-exp.
 LSE_TOL = 1e-2
 
