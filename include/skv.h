@@ -17,7 +17,9 @@
  *
  * Conventions shared by every call:
  *  - All pointers named "device" are CUDA device pointers owned by the
- *    caller.  The library never allocates, never frees and never keeps a
+ *    caller, in memory of the device that is current when the call is made
+ *    (the kernels launch there; the library does not check where a pointer
+ *    lives).  The library never allocates, never frees and never keeps a
  *    pointer after a call returns.
  *  - bf16 tensors are raw 16-bit brain-float arrays, C-contiguous, in the
  *    layout stated beside them; every device pointer must be 16-byte

@@ -93,6 +93,8 @@ def _check(rc: int, what: str):
 
 
 def _stream():
+    """The current torch stream of the current device: the library launches
+    on the current device, so the tensors of a call must live there."""
     return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
 
 
