@@ -282,6 +282,8 @@ size_t skv_verify_workspace_bytes(const skv_cache* cache, int32_t n_q_head, int3
  * ws: device workspace of ws_bytes >= skv_verify_workspace_bytes(); it must
  *     be zero-filled before its first use, the call leaves it ready for the
  *     next one (re-zero it after a call that set a device status bit).
+ *     Calls that may run at the same time (other streams) need workspaces
+ *     of their own: the arrival counters in it are per call.
  * Needs 1 <= blk <= tail_cap, V <= 64 and Hq/Hkv <= 64 (else
  * SKV_ERR_UNSUPPORTED); a block of more than 64 rows per kv head
  * (blk * Hq/Hkv) is taken 64 rows at a time, which needs Hq/Hkv to divide
