@@ -27,6 +27,15 @@
  *  - `stream` is a cudaStream_t passed as void*.  Calls only enqueue work on
  *    it, never synchronise and never copy to or from the host, so they may
  *    be captured into a CUDA graph.
+ *  - The attention calls rotate Q and K in fp32 and hand the tensor cores
+ *    fp16 operands (11 significant bits, 3 more than bf16).  fp16's largest
+ *    finite value is 65504: a rotated component beyond it is clamped to
+ *    +-65504, with no status bit.  The rotation keeps the length of every
+ *    (x_i, x_{i+d/2}) pair, so Q and K whose components all lie within
+ *    +-46000 (65504 / sqrt 2) never reach the clamp.  Components under
+ *    2^-14 in magnitude are fp16 subnormals and keep fewer bits.  The softmax
+ *    scale is applied in fp32 after the product, so large K with a small
+ *    sm_scale stays exact up to that rounding.
  *  - A call returns SKV_OK after enqueueing, or a negative SKV_ERR_* code
  *    and enqueues nothing.  Errors found on the device while the kernels run
  *    (a bounded wait that gave up, a ring head out of range, a tail that
@@ -79,7 +88,8 @@ extern "C" {
  *                                       products read K-major operands
  * head    device int32 [C][V]   ring heads (0 for an empty cache)
  * sync    device int32 [C][V]   zero-initialised counters used by
- *                               kv_stream_insert; the call leaves them at 0
+ *                               kv_stream_insert; the call leaves them at 0.
+ *                               No other call reads them: those accept NULL
  * rope    device fp32 [rope_len][d/2][2]  (cos, sin) of position*theta^(-2i/d),
  *                               filled by skv_build_rope_table; rope_len must
  *                               cover every logical index (P + V*F*T + tail_cap)
@@ -173,6 +183,9 @@ int kv_stream_insert(const skv_cache* cache, const void* k_new, const void* v_ne
  *
  * The first call on a device looks up the array's device address, with
  * that device current; make that first call before any stream capture.
+ * The address is kept for the life of the process: after a
+ * cudaDeviceReset of that device it is stale, so do not call this again
+ * in a process that reset the device.
  * Every call first clears the counters it uses with an asynchronous memset
  * on `stream`; it calls no cudaMalloc, cudaFree or allocating library
  * routine.  All calls on one device share the one array and it keeps what

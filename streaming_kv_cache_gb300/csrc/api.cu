@@ -3,6 +3,8 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <atomic>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "skv.h"
@@ -18,23 +20,27 @@ int cuda_fail(cudaError_t e) {
 
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
-// 1 = sm_103 device, -1 = other device; cached per device ordinal.
-int g_dev_ok[64];
+// 1 = sm_103 device, -1 = other device, 0 = not asked yet; cached per
+// device ordinal (host threads may fill an entry at the same time: they
+// store the same value, and the atomic makes that well defined).
+std::atomic<int> g_dev_ok[64];
 
 int check_device() {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e);
   if (dev < 0 || dev >= 64) return SKV_ERR_UNSUPPORTED;
-  if (g_dev_ok[dev] == 0) {
+  int ok = g_dev_ok[dev].load(std::memory_order_relaxed);
+  if (ok == 0) {
     int major = 0, minor = 0;
     if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess)
       return cuda_fail(e);
     if ((e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess)
       return cuda_fail(e);
-    g_dev_ok[dev] = (major == 10 && minor == 3) ? 1 : -1;
+    ok = (major == 10 && minor == 3) ? 1 : -1;
+    g_dev_ok[dev].store(ok, std::memory_order_relaxed);
   }
-  return g_dev_ok[dev] == 1 ? SKV_OK : SKV_ERR_UNSUPPORTED;
+  return ok == 1 ? SKV_OK : SKV_ERR_UNSUPPORTED;
 }
 
 int check_cache(const skv_cache* c) {
@@ -49,10 +55,16 @@ int check_cache(const skv_cache* c) {
   if (c->row_cap < need || (c->row_cap & 7) != 0) return SKV_ERR_INVALID;
   if (c->rope_len < need) return SKV_ERR_INVALID;
   if (c->n_cache == 0) return SKV_OK;  // nothing to touch: calls return early
-  if (!c->k || !c->vt || !c->head || !c->sync || !c->rope || !c->status) return SKV_ERR_INVALID;
+  if (!c->k || !c->vt || !c->head || !c->rope || !c->status) return SKV_ERR_INVALID;
   if (!aligned16(c->k) || !aligned16(c->vt) || !aligned16(c->rope)) return SKV_ERR_INVALID;
-  if (((uintptr_t)c->head & 3u) || ((uintptr_t)c->sync & 3u) || ((uintptr_t)c->status & 3u))
-    return SKV_ERR_INVALID;
+  if (((uintptr_t)c->head & 3u) || ((uintptr_t)c->status & 3u)) return SKV_ERR_INVALID;
+  return SKV_OK;
+}
+
+// The frame insert's arrival counters: only kv_stream_insert reads cache->sync.
+int check_sync(const skv_cache* c) {
+  if (c->n_cache == 0) return SKV_OK;
+  if (!c->sync || ((uintptr_t)c->sync & 3u)) return SKV_ERR_INVALID;
   return SKV_OK;
 }
 
@@ -76,8 +88,9 @@ int check_prefill_shape(const skv_cache* c, long long n_query, int n_q_head) {
 
 namespace skv {
 
-// The argument checks kv_stream_insert makes, without enqueueing anything;
-// lets a caller validate before it enqueues work of its own.
+// The argument checks kv_stream_insert makes, except those of cache->sync,
+// without enqueueing anything; lets a caller validate before it enqueues
+// work of its own.
 int check_insert_args(const skv_cache* cache, const void* k_new, const void* v_new) {
   int rc = check_cache(cache);
   if (rc) return rc;
@@ -145,6 +158,7 @@ int kv_write_rows(const skv_cache* cache, int32_t row0, int32_t n_rows, const vo
 int kv_stream_insert(const skv_cache* cache, const void* k_new, const void* v_new, void* stream) {
   int rc = check_cache(cache);
   if (rc) return rc;
+  if ((rc = check_sync(cache))) return rc;
   if (cache->n_cache == 0) return SKV_OK;
   if (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new)) return SKV_ERR_INVALID;
   if ((rc = check_device())) return rc;

@@ -103,39 +103,6 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   return d;
 }
 
-// 2^x of two values on the FMA pipe, to take part of the softmax's
-// exponentials off the quarter-rate special-function unit.  Cody-Waite
-// reduction x = j + f: adding 1.5*2^23 with rounding toward minus infinity
-// leaves j = floor(x) in the low mantissa bits, f = x - j lies in [0, 1).
-// 2^f is a degree-3 polynomial with 2^0 exact whose coefficients minimise the
-// largest relative error on [0, 1] (a linear-programming fit on 4001 points:
-// 8.6e-5, far below the 2^-9 rounding of a bf16 probability); 2^j is then
-// added into the exponent field.  x is clamped at -127, where the result is
-// 0 or a subnormal below 2^-126; callers never pass x above a few units.
-__device__ __forceinline__ void exp2_fma_x2(float x0, float x1, float& y0, float& y1) {
-  const uint64_t x = f2_pack(fmaxf(x0, -127.f), fmaxf(x1, -127.f));
-  const uint64_t magic = f2_pack(12582912.f, 12582912.f);
-  uint64_t t, j, f;
-  asm("add.rm.ftz.f32x2 %0, %1, %2;" : "=l"(t) : "l"(x), "l"(magic));
-  asm("sub.rn.ftz.f32x2 %0, %1, %2;" : "=l"(j) : "l"(t), "l"(magic));
-  asm("sub.rn.ftz.f32x2 %0, %1, %2;" : "=l"(f) : "l"(x), "l"(j));
-  uint64_t p = f2_fma(f2_pack(0.07706724107265472f, 0.07706724107265472f), f,
-                      f2_pack(0.22764497995376587f, 0.22764497995376587f));
-  p = f2_fma(p, f, f2_pack(0.6951166391372681f, 0.6951166391372681f));
-  p = f2_fma(p, f, f2_pack(1.f, 1.f));
-  float t0, t1, p0, p1;
-  f2_unpack(t, t0, t1);
-  f2_unpack(p, p0, p1);
-  y0 = __uint_as_float(__float_as_uint(p0) + (__float_as_uint(t0) << 23));
-  y1 = __uint_as_float(__float_as_uint(p1) + (__float_as_uint(t1) << 23));
-}
-
-// Whether pair q (0..15) of a 32-score chunk takes exp2_fma_x2 when n_fma
-// of the 16 pairs do: an even spread, so both pipes stay busy.
-__host__ __device__ constexpr bool fma_exp_pair(int q, int n_fma) {
-  return (q * n_fma) / 16 != ((q + 1) * n_fma) / 16;
-}
-
 __device__ __forceinline__ void set_status(int32_t* status, int bits) {
   if (status) atomicOr(status, bits);
 }

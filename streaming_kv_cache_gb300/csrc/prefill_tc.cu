@@ -46,6 +46,8 @@
 #include <cudaTypedefs.h>
 #include <math.h>
 
+#include <atomic>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "rope.cuh"
@@ -67,8 +69,6 @@ static_assert(256 * REG_SOFTMAX + 128 * REG_CTRL + 128 * REG_ROPE == 65536, "reg
 constexpr int MAX_TILES = 1024;
 constexpr int MAX_VIEWS = 64;
 constexpr float LAG_LIMIT = 1048576.0f;   // 2^20: a tile's probability sum that triggers a rescale
-// pairs of every 16 in a 32-score chunk whose exponentials run on the FMA pipe
-constexpr int FMA_EXP_PAIRS = 0;
 constexpr uint64_t DRAIN_NS = 500000000ull;  // bounded wait for own in-flight copies/MMAs
 
 template <int D>
@@ -617,13 +617,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
             float x0, x1;
             f2_unpack(f2_fma(f2_pack(__uint_as_float(v[cb * 32 + k]), __uint_as_float(v[cb * 32 + k + 1])), sl2, nm2),
                       x0, x1);
-            float p0, p1;
-            if (fma_exp_pair(k >> 1, FMA_EXP_PAIRS)) {
-              exp2_fma_x2(x0, x1, p0, p1);
-            } else {
-              p0 = tc::ex2(x0);
-              p1 = tc::ex2(x1);
-            }
+            const float p0 = tc::ex2(x0), p1 = tc::ex2(x1);
             l2[(k >> 1) & 3] = f2_add(l2[(k >> 1) & 3], f2_pack(p0, p1));
             pk[k >> 1] = pack_bf16x2(p0, p1);
           }
@@ -713,15 +707,15 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
 // largest carve-out made the 36-layer call 3% slower).
 template <typename K>
 cudaError_t set_smem_once(K kernel, int bytes, int variant) {
-  static int done[64][4];
+  static std::atomic<int> done[64][4];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev >= 0 && dev < 64 && done[dev][variant]) return cudaSuccess;
+  if (dev >= 0 && dev < 64 && done[dev][variant].load(std::memory_order_relaxed)) return cudaSuccess;
   e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxL1);
-  if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev][variant] = 1;
+  if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev][variant].store(1, std::memory_order_relaxed);
   return e;
 }
 
@@ -732,14 +726,17 @@ cudaError_t set_smem_once(K kernel, int bytes, int variant) {
 // with the 128-byte swizzle.
 // cuTensorMapEncodeTiled from the driver, looked up once (no link against libcuda).
 PFN_cuTensorMapEncodeTiled_v12000 tmap_encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::atomic<PFN_cuTensorMapEncodeTiled_v12000> cached{nullptr};
+  PFN_cuTensorMapEncodeTiled_v12000 fn = cached.load(std::memory_order_relaxed);
   if (!fn) {
     void* ptr = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
             cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
+        q == cudaDriverEntryPointSuccess) {
       fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+      cached.store(fn, std::memory_order_relaxed);
+    }
   }
   return fn;
 }

@@ -36,6 +36,8 @@
 #include <cudaTypedefs.h>
 #include <math.h>
 
+#include <atomic>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "rope.cuh"
@@ -59,8 +61,6 @@ constexpr int MAX_PIECES = 16;   // pieces of one CTA's share
 constexpr int MAX_SPLITS = 64;   // pieces of one unit
 constexpr int MIN_SHARE = 4;     // key tiles per CTA at least
 constexpr float RESCALE_THRESHOLD = 8.0f;
-// pairs of every 16 in a 32-score chunk whose exponentials run on the FMA pipe
-constexpr int FMA_EXP_PAIRS = 0;
 constexpr uint64_t DRAIN_NS = 500000000ull;
 
 template <int D>
@@ -437,7 +437,8 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
     // of the next tile, BN rows on inside the same run, is this tile's first
     // row turned by R(BN), no table load
     float4* s_r64 = reinterpret_cast<float4*>(smem + L::R64_OFF) + wr * NCH * 4;
-    if (ln < NCH * 4) s_r64[ln] = __ldg(rope4 + ((size_t)BN * HALF + (ln / 4) * 8) / 2 + ln % 4);
+    // (a table of at most BN rows has no run longer than BN to turn along)
+    if (ln < NCH * 4 && g.rope_len > BN) s_r64[ln] = __ldg(rope4 + ((size_t)BN * HALF + (ln / 4) * 8) / 2 + ln % 4);
     __syncwarp();
     int gt = 0, a = 0;
     bool ok = true, q_in_flight = false;
@@ -619,13 +620,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
             float x0, x1;
             f2_unpack(f2_fma(f2_pack(__uint_as_float(v[cb * 32 + k]), __uint_as_float(v[cb * 32 + k + 1])), sl2, nm2),
                       x0, x1);
-            float p0, p1;
-            if (fma_exp_pair(k >> 1, FMA_EXP_PAIRS)) {
-              exp2_fma_x2(x0, x1, p0, p1);
-            } else {
-              p0 = tc::ex2(x0);
-              p1 = tc::ex2(x1);
-            }
+            const float p0 = tc::ex2(x0), p1 = tc::ex2(x1);
             l2[(k >> 1) & 3] = f2_add(l2[(k >> 1) & 3], f2_pack(p0, p1));
             pk[k >> 1] = pack_bf16x2(p0, p1);
           }
@@ -735,29 +730,30 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
   }
 }
 
-int g_num_sms[64];
+// SM count per device ordinal, asked once (threads that race store the same value)
+std::atomic<int> g_num_sms[64];
 
 int num_sms() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
-  if (!g_num_sms[dev]) {
-    int n = 0;
+  int n = g_num_sms[dev].load(std::memory_order_relaxed);
+  if (!n) {
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
-    g_num_sms[dev] = n;
+    g_num_sms[dev].store(n, std::memory_order_relaxed);
   }
-  return g_num_sms[dev];
+  return n;
 }
 
 // Raise the kernel's dynamic shared-memory limit once per device.
 template <typename K>
 cudaError_t set_smem_once(K kernel, int bytes, int variant) {
-  static int done[64][4];
+  static std::atomic<int> done[64][4];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev >= 0 && dev < 64 && done[dev][variant]) return cudaSuccess;
+  if (dev >= 0 && dev < 64 && done[dev][variant].load(std::memory_order_relaxed)) return cudaSuccess;
   e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-  if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev][variant] = 1;
+  if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev][variant].store(1, std::memory_order_relaxed);
   return e;
 }
 

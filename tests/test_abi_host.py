@@ -65,7 +65,7 @@ def _desc(**kw):
 @pytest.mark.parametrize("bad", [
     dict(head_dim=96), dict(head_dim=0), dict(n_view=0), dict(n_frame=0), dict(frame_len=0),
     dict(prefix_len=-1), dict(tail_cap=-1), dict(n_kv_head=0), dict(row_cap=3200),
-    dict(row_cap=3330), dict(rope_len=3000), dict(k=0), dict(vt=0), dict(head=0), dict(sync=0),
+    dict(row_cap=3330), dict(rope_len=3000), dict(k=0), dict(vt=0), dict(head=0),
     dict(rope=0), dict(status=0), dict(k=FAKE + 8), dict(vt=FAKE + 2), dict(head=FAKE + 2),
 ])
 def test_bad_cache_descriptor_is_rejected(L, bad):
@@ -73,6 +73,27 @@ def test_bad_cache_descriptor_is_rejected(L, bad):
     p = ctypes.c_void_p
     assert L.kv_stream_insert(ctypes.byref(d), p(FAKE), p(FAKE), None) == skv.SKV_ERR_INVALID
     assert L.stream_attn_prefill(ctypes.byref(d), 32, p(FAKE), p(FAKE), None, 1.0, None) == skv.SKV_ERR_INVALID
+
+
+def test_sync_counters_are_needed_by_the_insert_only(L):
+    """cache->sync holds the frame insert's arrival counters: kv_stream_insert
+    rejects a null or misaligned one, every other call accepts a descriptor
+    without it (here they get past every argument check and stop only at
+    the missing GPU)."""
+    p = ctypes.c_void_p
+    for sync in (0, FAKE + 2):
+        r = ctypes.byref(_desc(sync=sync))
+        assert L.kv_stream_insert(r, p(FAKE), p(FAKE), None) == skv.SKV_ERR_INVALID
+    r = ctypes.byref(_desc(sync=0))
+    no_gpu = (skv.SKV_ERR_CUDA, skv.SKV_ERR_UNSUPPORTED)
+    assert L.stream_attn_prefill(r, 32, p(FAKE), p(FAKE), None, 1.0, None) in no_gpu
+    assert L.stream_attn_window(r, 32, p(FAKE), p(FAKE), None, 1.0, None) in no_gpu
+    assert L.stream_attn_prefill_tail(r, 32, 9, *[p(FAKE)] * 5, None, 1.0, None) in no_gpu
+    assert L.kv_write_rows(r, 0, 8, p(FAKE), p(FAKE), None) in no_gpu
+    ws = L.skv_verify_workspace_bytes(r, 32, 9)
+    assert ws > 0
+    assert L.stream_attn_verify(r, 32, 9, *[p(FAKE)] * 5, None, None, None, None, p(FAKE), ws, 1.0,
+                                None) in no_gpu
 
 
 def test_null_descriptor(L):

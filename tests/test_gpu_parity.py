@@ -8,7 +8,7 @@ import torch
 from oracle import skv_oracle as O
 from streaming_kv_cache_gb300 import skv, synth
 
-from gpu_harness import Pair, assert_close, bf16_dev_to_f64, from_dev, to_dev
+from gpu_harness import Pair, assert_close, assert_lse, bf16_dev_to_f64, from_dev, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -39,8 +39,7 @@ def _prefill_check(pair, step_tag, rows=None, watch=None, lse_tol=LSE_TOL, rel=0
         want, wl = O.stream_prefill(pair.win[c], q[c], w.theta, w.sm_scale, rows=rows)
         sel = slice(None) if rows is None else rows
         assert_close(got[c][sel], want, "%s cache %d" % (w.name, c), rel=rel, max_abs=max_abs)
-        err = np.abs(got_lse[c][:, sel].T - wl).max()
-        assert err < lse_tol, "lse err %g" % err
+        assert_lse(got_lse[c][:, sel].T, wl, lse_tol, "%s cache %d" % (w.name, c))
     assert pair.cache.device_status() == 0
     return got
 
@@ -75,17 +74,32 @@ def test_alpamayo_20_streaming_steps():
         _prefill_check(pair, "s%d" % s)
 
 
-def test_prefill_scaleup_36_layers_sampled():
+def test_prefill_scaleup_36_layers():
+    """The scale-up workload in the launch the bench times (36 layer caches
+    in one call): every query row and head of the first and the last layer
+    cache element by element, and sampled rows (tile edges, frame edges,
+    random rows) of every one of the 36."""
     w = W["scaleup_36L"]
-    watch = [0, 17, 35]
-    pair = Pair(w, "big", watch=watch)
+    pair = Pair(w, "big")
     pair.fill()
     pair.insert()
     pair.check_ring()
+    q = synth.frame_q(w, pair.n_inserts - 1, pair.tag + "x")
+    out, lse = skv.stream_attn_prefill(pair.cache, to_dev(q), w.sm_scale, lse=True)
+    got = bf16_dev_to_f64(out)
+    got_lse = lse.cpu().numpy()
+    assert pair.cache.device_status() == 0
     rng = np.random.default_rng(5)
-    rows = sorted(set([0, 1, w.T - 1, w.T, 2 * w.T + 7, w.n_new - 1]
-                      + list(rng.integers(0, w.n_new, 26))))
-    _prefill_check(pair, "x", rows=np.array(rows), watch=watch)
+    sampled = np.array(sorted(set([0, 1, 127, 128, w.T - 1, w.T, 2 * w.T + 7, w.n_new - 1]
+                                  + list(rng.integers(0, w.n_new, 8)))))
+    for c in range(w.C):
+        whole = c in (0, w.C - 1)
+        # whole caches in chunks of rows, to bound the oracle's memory
+        chunks = np.array_split(np.arange(w.n_new), 6) if whole else [sampled]
+        for rows in chunks:
+            want, wl = O.stream_prefill(pair.win[c], q[c], w.theta, w.sm_scale, rows=rows)
+            assert_close(got[c][rows], want, "scale-up cache %d rows %d..%d" % (c, rows[0], rows[-1]))
+            assert_lse(got_lse[c][:, rows].T, wl, LSE_TOL, "scale-up cache %d" % c)
 
 
 def test_prefill_peaky_queries():

@@ -11,7 +11,7 @@ import torch
 from oracle import skv_oracle as O
 from streaming_kv_cache_gb300 import skv, synth
 
-from gpu_harness import Pair, assert_close, bf16_dev_to_f64, from_dev, to_dev
+from gpu_harness import Pair, assert_close, assert_lse, bf16_dev_to_f64, from_dev, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -52,7 +52,7 @@ def _tail_check(pair, tail, n, tag):
     for c, win in pair.win.items():
         want, wl = O.stream_prefill_tail(win, q[c], k[c], v[c], w.theta, w.sm_scale)
         assert_close(got[c], want, "%s tail n=%d cache %d" % (w.name, n, c))
-        assert np.abs(got_lse[c].T - wl).max() < LSE_TOL
+        assert_lse(got_lse[c].T, wl, LSE_TOL, "%s tail cache %d" % (w.name, c))
         base = pair.cache.n_visual + int(tails[c])
         np.testing.assert_array_equal(kk[c][:, base:base + n].transpose(1, 0, 2), k[c])
         np.testing.assert_array_equal(vt[c][:, :, base:base + n].transpose(2, 0, 1), v[c])
@@ -134,7 +134,7 @@ def _window_check(pair, tag, rows=None):
     for c, win in pair.win.items():
         want, wl = O.stream_window(win, q[c], w.theta, w.sm_scale, rows=rows)
         assert_close(got[c][sel], want, "%s window cache %d" % (w.name, c))
-        assert np.abs(got_lse[c][:, sel].T - wl).max() < LSE_TOL
+        assert_lse(got_lse[c][:, sel].T, wl, LSE_TOL, "%s window cache %d" % (w.name, c))
     assert pair.cache.device_status() == 0
 
 
@@ -177,6 +177,25 @@ def test_window_scaleup_sampled_rows():
             rows += [b, b + 127, b + 128, b + w.T - 1]
     rows = np.array(sorted(set(rows + [w.n_window - 1])))
     _window_check(pair, "a", rows=rows)
+
+
+def test_window_scaleup_whole_cache():
+    """Every one of the 12,800 window tokens of one scale-up cache (turned
+    ring), all heads, element by element; the oracle works through the rows
+    in chunks to bound its memory."""
+    w = W["scaleup_36L"].with_(C=2)
+    pair = Pair(w, "wsw", watch=[0])
+    pair.fill()
+    pair.insert()
+    q = synth.window_q(w, pair.tag + "a")
+    out, lse = skv.stream_attn_window(pair.cache, to_dev(q), w.sm_scale, lse=True)
+    got, got_lse = bf16_dev_to_f64(out), lse.cpu().numpy()
+    assert pair.cache.device_status() == 0
+    win = pair.win[0]
+    for rows in np.array_split(np.arange(w.n_window), 16):
+        want, wl = O.stream_window(win, q[0], w.theta, w.sm_scale, rows=rows)
+        assert_close(got[0][rows], want, "scale-up window rows %d..%d" % (rows[0], rows[-1]))
+        assert_lse(got_lse[0][:, rows].T, wl, LSE_TOL, "scale-up window")
 
 
 WINDOW_GEOMETRIES = [

@@ -30,6 +30,9 @@ def test_noalloc_insert_matches_insert_on_two_calls():
     for c in caches:
         skv.kv_write_rows(c, 0, _dev(pk), _dev(pv))
     ref, new = caches
+    # a sentinel in the cache's own counter tensor: the descriptor handed to
+    # the no-alloc call carries no sync pointer, so these must stay untouched
+    new.sync.fill_(0x5A5A)
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
     for i in range(w.F + 2):          # fills the window, then two streaming steps
         k, v = synth.frame_kv(w, i, "na")
@@ -46,7 +49,7 @@ def test_noalloc_insert_matches_insert_on_two_calls():
         assert torch.equal(ref.vt, new.vt), i
         assert torch.equal(ref.head, new.head), i
         assert new.device_status() == 0 and ref.device_status() == 0
-    assert (new.sync == 0).all()         # the caller's own counters were never touched
+    assert (new.sync == 0x5A5A).all()    # the cache's own counters were never touched
 
 
 def test_noalloc_insert_rejects_too_many_counters():
