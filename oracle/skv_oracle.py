@@ -64,6 +64,79 @@ def rope_rotate(x: np.ndarray, pos: np.ndarray, theta: float) -> np.ndarray:
 
 
 # ---------------------------------------------------------------------------
+# multi-section rotary: a stated reading.  [FD-news] names a Qwen3-VL
+# backbone, whose vision tokens carry (temporal, height, width) positions,
+# and [FD-blog] 3.3 lost the rotary formula, so this form is not printed on
+# the pages.  Reading: a token has a position triple (t, h, w).  Tokens that
+# are not camera tokens (prefix, tail, blocks) have t = h = w = their logical
+# index n, so they rotate exactly as in rope_rotate.  The T tokens of a frame
+# form rows of W tokens in raster order; token tau of a frame whose first
+# token sits at logical index b has t = b, h = b + (tau // W), w = b + (tau %
+# W).  Frequency i (of the d/2) turns by the component sec[i] (0 = t, 1 = h,
+# 2 = w) times theta^(-2i/d).  Positions still shift as frames age, because b
+# is a logical index.
+
+def interleaved_sections(d: int, n_h: int, n_w: int) -> np.ndarray:
+    """Frequency -> component map: the d/2 frequencies are dealt to t, h, w
+    in turn (frequency i gets component i mod 3) while h and w still have
+    frequencies left of their shares n_h and n_w; every other frequency
+    belongs to t."""
+    sec = np.zeros(d // 2, dtype=np.int64)
+    for i in range(d // 2):
+        c, k = i % 3, i // 3
+        if (c == 1 and k < n_h) or (c == 2 and k < n_w):
+            sec[i] = c
+    return sec
+
+
+class MRope:
+    """The multi-section reading for one window geometry: P prefix tokens,
+    V views of F frames of T tokens in rows of W, and the frequency map sec."""
+
+    def __init__(self, P, V, F, T, W, sec):
+        assert T % W == 0
+        self.P, self.V, self.F, self.T, self.W = P, V, F, T, W
+        self.sec = np.asarray(sec, dtype=np.int64)
+
+    def triples(self, idx) -> np.ndarray:
+        """Position triples [n][3] (t, h, w) of the tokens at logical
+        indices idx."""
+        out = []
+        for n in np.asarray(idx, dtype=np.int64).reshape(-1):
+            n = int(n)
+            if self.P <= n < self.P + self.V * self.F * self.T:
+                tau = (n - self.P) % self.T
+                b = n - tau
+                out.append((b, b + tau // self.W, b + tau % self.W))
+            else:
+                out.append((n, n, n))
+        return np.array(out, dtype=np.int64).reshape(-1, 3)
+
+
+def rope_rotate_sections(x: np.ndarray, triples: np.ndarray, theta: float, sec: np.ndarray) -> np.ndarray:
+    """Rotate rows of x ([..., n, d], fp64) by position triples [n][3]: the
+    pair (x_i, x_{i+d/2}) turns by triples[n, sec[i]] * theta^(-2i/d), in the
+    rotate-half form of rope_rotate."""
+    x = np.asarray(x, dtype=np.float64)
+    d = x.shape[-1]
+    i = np.arange(d // 2, dtype=np.float64)
+    freq = np.power(float(theta), -2.0 * i / d)                     # theta^(-2i/d)
+    comp = np.asarray(triples, dtype=np.float64)[:, np.asarray(sec, dtype=np.int64)]   # [n][d/2]
+    ang = comp * freq[None, :]
+    cos, sin = np.cos(ang), np.sin(ang)
+    lo, hi = x[..., : d // 2], x[..., d // 2:]
+    return np.concatenate([lo * cos - hi * sin, hi * cos + lo * sin], axis=-1)
+
+
+def _rotate(x, pos, theta, mrope):
+    """rope_rotate at logical positions, or the multi-section rotation of
+    the tokens at those logical indices when a reading is given."""
+    if mrope is None:
+        return rope_rotate(x, pos, theta)
+    return rope_rotate_sections(x, mrope.triples(pos), theta, mrope.sec)
+
+
+# ---------------------------------------------------------------------------
 # the logical sliding window ([FD-blog] 3.1 and 3.2; [FD-summary] "Streaming
 # Inference")
 
@@ -154,13 +227,15 @@ class StreamWindow:
 # attention ([FD-blog] 3.2: standard attention with mask M; a query sees a key
 # iff the key's logical index is at most the query's)
 
-def attention_rows(q_bits, q_pos, k_bits, v_bits, k_pos, theta, sm_scale):
+def attention_rows(q_bits, q_pos, k_bits, v_bits, k_pos, theta, sm_scale, mrope=None):
     """Masked softmax attention of selected query rows over a key sequence.
 
     q_bits [n][Hq][d] pre-RoPE queries at logical positions q_pos [n];
     k_bits, v_bits [N][Hkv][d] pre-RoPE keys / values at positions k_pos [N].
     Query head h uses key/value head floor(h / (Hq/Hkv)).
     Score = <R(q_pos) q, R(k_pos) k> * sm_scale, kept iff k_pos <= q_pos.
+    With mrope (an MRope reading) the rotation is the multi-section one of
+    the tokens at those logical indices; the mask stays on logical indices.
     Returns O [n][Hq][d] (fp64) and the natural-log LSE [n][Hq] of the
     scaled scores.
     """
@@ -173,9 +248,9 @@ def attention_rows(q_bits, q_pos, k_bits, v_bits, k_pos, theta, sm_scale):
     q_pos = np.asarray(q_pos, dtype=np.int64)
     k_pos = np.asarray(k_pos, dtype=np.int64)
     visible = k_pos[None, :] <= q_pos[:, None]                     # [n][N]
-    kr = rope_rotate(np.transpose(k, (1, 0, 2)), k_pos, theta)     # [Hkv][N][d]
+    kr = _rotate(np.transpose(k, (1, 0, 2)), k_pos, theta, mrope)  # [Hkv][N][d]
     vt = np.transpose(v, (1, 0, 2))                                # [Hkv][N][d]
-    qr = rope_rotate(np.transpose(q, (1, 0, 2)), q_pos, theta)     # [Hq][n][d]
+    qr = _rotate(np.transpose(q, (1, 0, 2)), q_pos, theta, mrope)  # [Hq][n][d]
     out = np.zeros((Hq, n, d))
     lse = np.zeros((Hq, n))
     for h in range(Hq):
@@ -193,7 +268,7 @@ def attention_rows(q_bits, q_pos, k_bits, v_bits, k_pos, theta, sm_scale):
 # ---------------------------------------------------------------------------
 # the three steps of the path
 
-def stream_prefill(win: StreamWindow, q_new, theta, sm_scale, rows=None):
+def stream_prefill(win: StreamWindow, q_new, theta, sm_scale, rows=None, mrope=None):
     """New-frame queries against the full window ([FD-blog] 3.2, 3.3).
 
     q_new [V*T][Hq][d] pre-RoPE bits, token j = (view j // T, token j % T) of
@@ -209,10 +284,10 @@ def stream_prefill(win: StreamWindow, q_new, theta, sm_scale, rows=None):
     q_pos = np.array([win.new_frame_index(int(j) // win.T, int(j) % win.T) for j in rows])
     k_bits, v_bits = win.logical_kv(with_tail=False)
     k_pos = np.arange(k_bits.shape[0])
-    return attention_rows(q_new[rows], q_pos, k_bits, v_bits, k_pos, theta, sm_scale)
+    return attention_rows(q_new[rows], q_pos, k_bits, v_bits, k_pos, theta, sm_scale, mrope)
 
 
-def _block_after_tail(win: StreamWindow, blk_q, blk_k, blk_v, theta, sm_scale):
+def _block_after_tail(win: StreamWindow, blk_q, blk_k, blk_v, theta, sm_scale, mrope=None):
     """Tokens appended after the window's tail, as queries: token j sits at
     logical index n_visual + tail_len + j and sees the prefix, all frames, the
     whole tail and block tokens 0..j.  blk_q [n][Hq][d], blk_k/blk_v
@@ -225,10 +300,10 @@ def _block_after_tail(win: StreamWindow, blk_q, blk_k, blk_v, theta, sm_scale):
     k_pos = np.arange(k_all.shape[0])
     q_pos = base + np.arange(blk)
     return attention_rows(np.asarray(blk_q, np.uint16), q_pos, k_all, v_all, k_pos,
-                          theta, sm_scale)
+                          theta, sm_scale, mrope)
 
 
-def stream_verify(win: StreamWindow, blk_q, blk_k, blk_v, theta, sm_scale):
+def stream_verify(win: StreamWindow, blk_q, blk_k, blk_v, theta, sm_scale, mrope=None):
     """Speculative-verify block ([FD-blog] 4.2 steps 1-2; [VFlash] "03 ·
     Generalist decoding": the target checks a whole drafted block in one
     pass).
@@ -238,10 +313,10 @@ def stream_verify(win: StreamWindow, blk_q, blk_k, blk_v, theta, sm_scale):
     and block tokens 0..j.  blk_q [blk][Hq][d], blk_k/blk_v [blk][Hkv][d].
     Returns (O [blk][Hq][d], LSE [blk][Hq]).
     """
-    return _block_after_tail(win, blk_q, blk_k, blk_v, theta, sm_scale)
+    return _block_after_tail(win, blk_q, blk_k, blk_v, theta, sm_scale, mrope)
 
 
-def stream_prefill_tail(win: StreamWindow, tail_q, tail_k, tail_v, theta, sm_scale):
+def stream_prefill_tail(win: StreamWindow, tail_q, tail_k, tail_v, theta, sm_scale, mrope=None):
     """Trajectory / text tokens after the views as queries ([FD-blog] 3.2
     "View-Major Ordering": the trailing trajectory and text tokens see every
     view and are causal among themselves; with the newest frames they are the
@@ -253,10 +328,10 @@ def stream_prefill_tail(win: StreamWindow, tail_q, tail_k, tail_v, theta, sm_sca
     tail_q [n][Hq][d], tail_k/tail_v [n][Hkv][d].  Returns (O, LSE).  The
     caller appends tail_k/tail_v to the window's tail afterwards.
     """
-    return _block_after_tail(win, tail_q, tail_k, tail_v, theta, sm_scale)
+    return _block_after_tail(win, tail_q, tail_k, tail_v, theta, sm_scale, mrope)
 
 
-def stream_window(win: StreamWindow, q_win, theta, sm_scale, rows=None):
+def stream_window(win: StreamWindow, q_win, theta, sm_scale, rows=None, mrope=None):
     """Every token of the window as a query: the first window of a stream,
     which only fills the cache ([FD-blog] 11 "Implementation Map": the first
     streaming window returns no trajectory), or a full re-encode.
@@ -273,7 +348,7 @@ def stream_window(win: StreamWindow, q_win, theta, sm_scale, rows=None):
     k_bits, v_bits = win.logical_kv(with_tail=False)
     n = k_bits.shape[0]
     rows = np.arange(n) if rows is None else np.asarray(rows)
-    return attention_rows(q_win[rows], rows, k_bits, v_bits, np.arange(n), theta, sm_scale)
+    return attention_rows(q_win[rows], rows, k_bits, v_bits, np.arange(n), theta, sm_scale, mrope)
 
 
 def accept_length(target_ids, draft_ids):

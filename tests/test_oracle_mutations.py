@@ -56,6 +56,23 @@ MUTATIONS = [
      "return k, target[k]", "return k, target[k - 1]"),
     ("bf16 widening shift",
      "<< np.uint32(16)", "<< np.uint32(15)"),
+    ("multi-section: rows and columns swapped",
+     "out.append((b, b + tau // self.W, b + tau % self.W))",
+     "out.append((b, b + tau % self.W, b + tau // self.W))"),
+    ("multi-section: temporal component from the token",
+     "out.append((b, b + tau // self.W, b + tau % self.W))",
+     "out.append((n, b + tau // self.W, b + tau % self.W))"),
+    ("multi-section: token offset without the prefix",
+     "tau = (n - self.P) % self.T", "tau = n % self.T"),
+    ("multi-section: frequencies not dealt in turn",
+     "c, k = i % 3, i // 3", "c, k = (i // 3) % 3, i % 3"),
+    ("multi-section: rotation sign",
+     "lo * cos - hi * sin, hi * cos + lo * sin", "lo * cos + hi * sin, hi * cos - lo * sin"),
+    ("multi-section: component order reversed",
+     "[:, np.asarray(sec, dtype=np.int64)]", "[:, 2 - np.asarray(sec, dtype=np.int64)]"),
+    ("multi-section: reading ignored by the attention",
+     "return rope_rotate_sections(x, mrope.triples(pos), theta, mrope.sec)",
+     "return rope_rotate(x, pos, theta)"),
 ]
 
 

@@ -622,3 +622,124 @@ def test_accept_extremes():
     assert O.accept_length(t, [0] + t[:8]) == (8, 13)       # all drafts accepted: bonus token
     assert O.accept_length(t, [0, 4] + t[1:8]) == (0, 5)    # first draft rejected
     assert O.accept_length(t, [t[0]] * 9) == (1, 6)         # slot 0 is never compared
+
+
+# --------------------------------------------------------------------------
+# multi-section rotary (a stated reading: position triples (t, h, w), the
+# frequencies dealt to the components in turn)
+
+def test_mrope_sections_are_dealt_in_turn():
+    sec = O.interleaved_sections(128, 20, 20)
+    assert len(sec) == 64
+    assert list(sec[:9]) == [0, 1, 2, 0, 1, 2, 0, 1, 2]
+    assert list(sec[60:]) == [0, 0, 0, 0]           # h and w shares used up: the rest is t
+    assert (sec == 1).sum() == 20 and (sec == 2).sum() == 20 and (sec == 0).sum() == 24
+    assert list(O.interleaved_sections(8, 1, 0)) == [0, 1, 0, 0]
+
+
+def test_mrope_triples_of_a_small_geometry():
+    """P=8, two views of two frames of 16 tokens in rows of 4: hand-listed."""
+    m = O.MRope(8, 2, 2, 16, 4, O.interleaved_sections(8, 1, 1))
+    want = {0: (0, 0, 0), 7: (7, 7, 7),              # prefix: t = h = w = n
+            8: (8, 8, 8),                           # view 0, frame 0, token 0
+            13: (8, 9, 9),                          # token 5: row 1, column 1
+            35: (24, 26, 27),                       # frame 1 starts at 24; token 11: row 2, column 3
+            40: (40, 40, 40),                       # view 1, frame 0, token 0
+            71: (56, 59, 59),                       # last window token: frame at 56, token 15
+            72: (72, 72, 72), 80: (80, 80, 80)}     # the tail after the window
+    got = m.triples(list(want))
+    for (n, tr), g in zip(want.items(), got):
+        assert tuple(g) == tr, n
+
+
+def test_mrope_equal_components_are_the_1d_rotation_bit_for_bit():
+    x = O.bf16_to_f64(_bits((2, 7, 64), 30))
+    pos = np.array([0, 1, 5, 99, 1000, 3137, 12799])
+    sec = O.interleaved_sections(64, 10, 10)
+    got = O.rope_rotate_sections(x, np.stack([pos, pos, pos], 1), 1e6, sec)
+    assert np.array_equal(got, O.rope_rotate(x, pos, 1e6))
+
+
+def test_mrope_hand_values():
+    """d = 6: three frequencies, one per component (t, h, w).  A unit vector
+    along pair i turns by the angle p_{sec(i)} * 16^(-2i/6)."""
+    sec = O.interleaved_sections(6, 1, 1)
+    assert list(sec) == [0, 1, 2]
+    tr = np.array([[2, 5, 7]])
+    for i in range(3):
+        x = np.zeros((1, 6))
+        x[0, i] = 1.0
+        y = O.rope_rotate_sections(x, tr, 16.0, sec)[0]
+        a = tr[0, i] * 16.0 ** (-2.0 * i / 6)
+        want = np.zeros(6)
+        want[i], want[i + 3] = math.cos(a), math.sin(a)
+        np.testing.assert_allclose(y, want, atol=1e-15)
+
+
+def test_mrope_a_component_moves_only_its_frequencies():
+    x = O.bf16_to_f64(_bits((1, 64), 31))
+    sec = O.interleaved_sections(64, 10, 10)
+    a = O.rope_rotate_sections(x, np.array([[40, 43, 45]]), 1e4, sec)[0]
+    b = O.rope_rotate_sections(x, np.array([[40, 43, 46]]), 1e4, sec)[0]     # only w moved
+    moved = np.abs(a - b) > 1e-12
+    pair = np.concatenate([sec, sec]) == 2
+    assert moved[pair].all() and not moved[~pair].any()
+
+
+def test_mrope_is_relative_in_every_component():
+    """Shifting both triples by the same (c_t, c_h, c_w) leaves the score."""
+    q = O.bf16_to_f64(_bits((1, 64), 32))
+    k = O.bf16_to_f64(_bits((1, 64), 33))
+    sec = O.interleaved_sections(64, 10, 10)
+    m, n = np.array([[300, 304, 311]]), np.array([[120, 121, 129]])
+    base = float((O.rope_rotate_sections(q, m, 1e4, sec) @ O.rope_rotate_sections(k, n, 1e4, sec).T)[0, 0])
+    for c in ([5, 0, 0], [0, 9, 0], [0, 0, 3], [7, 2, 11]):
+        c = np.array([c])
+        sh = float((O.rope_rotate_sections(q, m + c, 1e4, sec) @ O.rope_rotate_sections(k, n + c, 1e4, sec).T)[0, 0])
+        assert abs(sh - base) < 1e-9 * max(1.0, abs(base))
+
+
+def _brute_attention_mrope(q, qt, k, v, kt, q_idx, k_idx, sec, theta, scale):
+    """Scalar loop over rows, heads and keys; each frequency turns its pair
+    through a complex multiplication by its component of the triple; the
+    mask is on logical indices."""
+    n, Hq, d = q.shape
+    G = Hq // k.shape[1]
+    half = d // 2
+
+    def rot(vec, tr):
+        out = [0.0] * d
+        for i in range(half):
+            z = complex(vec[i], vec[i + half]) * cmath.exp(1j * tr[sec[i]] * theta ** (-2.0 * i / d))
+            out[i], out[i + half] = z.real, z.imag
+        return out
+
+    res = np.zeros((n, Hq, d))
+    for a in range(n):
+        for h in range(Hq):
+            qa = rot(list(q[a, h]), qt[a])
+            scores = [(sum(x * y for x, y in zip(qa, rot(list(k[b, h // G]), kt[b]))) * scale, b)
+                      for b in range(k.shape[0]) if k_idx[b] <= q_idx[a]]
+            mx = max(s for s, _ in scores)
+            w = [(math.exp(s - mx), b) for s, b in scores]
+            tot = sum(x for x, _ in w)
+            for x, b in w:
+                res[a, h] += x / tot * v[b, h // G]
+    return res
+
+
+def test_mrope_attention_matches_brute_force():
+    """Attention with the multi-section rotation over a small window: prefix
+    of 3, two views of two frames of 6 tokens in rows of 3, two tail tokens."""
+    m = O.MRope(3, 2, 2, 6, 3, O.interleaved_sections(8, 1, 1))
+    N = 3 + 2 * 2 * 6 + 2
+    qb, kb, vb = _bits((4, 4, 8), 34), _bits((N, 2, 8), 35), _bits((N, 2, 8), 36)
+    q_idx = np.array([4, 13, 26, 28])
+    k_idx = np.arange(N)
+    got, _ = O.attention_rows(qb, q_idx, kb, vb, k_idx, 50.0, 0.4, mrope=m)
+    want = _brute_attention_mrope(O.bf16_to_f64(qb), m.triples(q_idx), O.bf16_to_f64(kb), O.bf16_to_f64(vb),
+                                  m.triples(k_idx), q_idx, k_idx, m.sec, 50.0, 0.4)
+    np.testing.assert_allclose(got, want, rtol=1e-11, atol=1e-12)
+    # and it is not the 1-D rotation
+    one_d, _ = O.attention_rows(qb, q_idx, kb, vb, k_idx, 50.0, 0.4)
+    assert np.abs(one_d - got).max() > 1e-3
