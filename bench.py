@@ -362,7 +362,14 @@ def run_only(args):
         w = w.with_(tail_cap=max(w.tail_cap, args.tail_n))
     if args.only == "verify" and args.blk:
         w = w.with_(blk=args.blk)
-    cache = skv.StreamCache(w.C, w.P, w.V, w.F, w.T, w.Hkv, w.d, w.theta, tail_cap=w.tail_cap)
+    mrope = None
+    if args.mrope:
+        # multi-section rotary: frames in rows of --mrope tokens, 5/16 of the
+        # frequencies each on height and width, dealt in turn with temporal
+        n_hw = (w.d // 2) * 5 // 16
+        sec = [(i % 3 if i // 3 < n_hw else 0) for i in range(w.d // 2)]
+        mrope = (args.mrope, sec)
+    cache = skv.StreamCache(w.C, w.P, w.V, w.F, w.T, w.Hkv, w.d, w.theta, tail_cap=w.tail_cap, mrope=mrope)
     skv.kv_write_rows(cache, 0, randn((w.C, w.P, w.Hkv, w.d)), randn((w.C, w.P, w.Hkv, w.d)))
     k_new = randn((w.C, w.V, w.T, w.Hkv, w.d))
     for _ in range(w.F):
@@ -428,7 +435,7 @@ def run_only(args):
         ms.append(a.elapsed_time(b) / args.steps)
     status = cache.device_status()
     med = statistics.median(ms)
-    emit({"only": args.only, "layers_or_batch": w.C, "ms_median": med, "ms": ms,
+    emit({"only": args.only, "layers_or_batch": w.C, "mrope_grid_w": args.mrope, "ms_median": med, "ms": ms,
           "throughput": work / (med * 1e-3), "unit": unit, "device_status": status})
     if status:
         sys.exit(3)
@@ -447,6 +454,8 @@ def main():
                     help="layer caches (prefill/insert) or batch (verify) of the --only case")
     ap.add_argument("--tail-n", type=int, default=128,
                     help="tail tokens of the --only tail case (after an empty tail)")
+    ap.add_argument("--mrope", type=int, default=0,
+                    help="multi-section rotary on the --only case, frames in rows of this many tokens")
     ap.add_argument("--blk", type=int, default=None,
                     help="verify block size of the --only verify case (default: the workload's 9)")
     args = ap.parse_args()

@@ -90,9 +90,17 @@ extern "C" {
  * sync    device int32 [C][V]   zero-initialised counters used by
  *                               kv_stream_insert; the call leaves them at 0.
  *                               No other call reads them: those accept NULL
- * rope    device fp32 [rope_len][d/2][2]  (cos, sin) of position*theta^(-2i/d),
- *                               filled by skv_build_rope_table; rope_len must
- *                               cover every logical index (P + V*F*T + tail_cap)
+ * rope    device fp32 [rope_len][d/2][2]  rotary angles, read as rope_mode says;
+ *                               rope_len must cover every logical index
+ *                               (P + V*F*T + tail_cap)
+ *   rope_mode 0: row p holds (cos, sin) of p*theta^(-2i/d) (filled by
+ *                skv_build_rope_table): a token's position is its logical
+ *                index, and the kernels step the angles along runs of
+ *                consecutive positions (one table read per run);
+ *   rope_mode 1: row n holds the angles of the token at logical index n
+ *                under any per-token positions (filled, for the
+ *                multi-section reading, by skv_build_mrope_table): the
+ *                kernels read the row of every key and query.
  * status  device int32 [1]      SKV_DEV_* bits, OR-ed in by the kernels
  *
  * Every row of k and vt must hold finite values (allocate them zeroed):
@@ -116,6 +124,8 @@ typedef struct skv_cache {
   const float* rope;
   int32_t* status;
   uint64_t wait_ns;   /* limit of every bounded wait in a kernel; 0 = 2 s */
+  int32_t rope_mode;  /* 0 or 1, see rope above */
+  int32_t reserved;   /* 0 */
 } skv_cache;
 
 /* Library version (SKV_VERSION). */
@@ -140,6 +150,29 @@ int32_t skv_row_cap(int32_t P, int32_t V, int32_t F, int32_t T, int32_t tail_cap
  */
 int skv_build_rope_table(float* tab, int32_t n_pos, int32_t head_dim, double theta,
                          void* stream);
+
+/*
+ * Fill a rotary table for rope_mode 1 with the multi-section reading of the
+ * positions (FlashDrive's backbone is a Qwen3-VL model, whose vision tokens
+ * carry temporal, height and width positions; the pages print no rotary
+ * formula, so this is a stated reading, not the pages' text):
+ *  - a token that is not a camera token (prefix, tail, verify block) at
+ *    logical index n has the position triple (t, h, w) = (n, n, n);
+ *  - the T tokens of a frame form rows of grid_w tokens in raster order;
+ *    token tau of a frame whose first token sits at logical index b has
+ *    (t, h, w) = (b, b + tau / grid_w, b + tau % grid_w);
+ *  - frequency i (i < d/2) turns by the height component when bit i of
+ *    h_mask is set, by the width component when bit i of w_mask is set,
+ *    else by the temporal one: angle = component * theta^(-2i/d).
+ * Row n of tab holds (cos, sin) of those angles for the token at logical
+ * index n (n < n_pos); angles in fp64, rounded once to fp32.  The rows of
+ * tokens that are not camera tokens equal skv_build_rope_table's.
+ * tab: device fp32 [n_pos][d/2][2].  Needs head_dim/2 <= 64, T % grid_w == 0
+ * and no bit set in both masks (else SKV_ERR_INVALID).
+ */
+int skv_build_mrope_table(float* tab, int32_t n_pos, int32_t head_dim, double theta, int32_t P,
+                          int32_t V, int32_t F, int32_t T, int32_t grid_w, uint64_t h_mask,
+                          uint64_t w_mask, void* stream);
 
 /*
  * Write n_rows token-major K/V rows into rows [row0, row0 + n_rows) of every

@@ -54,6 +54,7 @@ int check_cache(const skv_cache* c) {
   if (need > 0x3FFFFFFFLL) return SKV_ERR_INVALID;
   if (c->row_cap < need || (c->row_cap & 7) != 0) return SKV_ERR_INVALID;
   if (c->rope_len < need) return SKV_ERR_INVALID;
+  if (c->rope_mode != 0 && c->rope_mode != 1) return SKV_ERR_INVALID;
   if (c->n_cache == 0) return SKV_OK;  // nothing to touch: calls return early
   if (!c->k || !c->vt || !c->head || !c->rope || !c->status) return SKV_ERR_INVALID;
   if (!aligned16(c->k) || !aligned16(c->vt) || !aligned16(c->rope)) return SKV_ERR_INVALID;
@@ -137,6 +138,22 @@ int skv_build_rope_table(float* tab, int32_t n_pos, int32_t head_dim, double the
   int rc = check_device();
   if (rc) return rc;
   cudaError_t e = skv::launch_rope_table(tab, n_pos, head_dim, theta, (cudaStream_t)stream);
+  return e == cudaSuccess ? SKV_OK : cuda_fail(e);
+}
+
+int skv_build_mrope_table(float* tab, int32_t n_pos, int32_t head_dim, double theta, int32_t P,
+                          int32_t V, int32_t F, int32_t T, int32_t grid_w, uint64_t h_mask,
+                          uint64_t w_mask, void* stream) {
+  if (!tab || n_pos < 1 || head_dim < 2 || (head_dim & 1) || head_dim / 2 > 64 || !(theta > 0.0) ||
+      !aligned16(tab))
+    return SKV_ERR_INVALID;
+  if (P < 0 || V < 1 || F < 1 || T < 1 || grid_w < 1 || T % grid_w || (h_mask & w_mask))
+    return SKV_ERR_INVALID;
+  if ((long long)P + (long long)V * F * T > 0x3FFFFFFFLL) return SKV_ERR_INVALID;
+  int rc = check_device();
+  if (rc) return rc;
+  skv::MRopeGeom m{P, V, F, T, grid_w, h_mask, w_mask};
+  cudaError_t e = skv::launch_mrope_table(tab, n_pos, head_dim, theta, m, (cudaStream_t)stream);
   return e == cudaSuccess ? SKV_OK : cuda_fail(e);
 }
 

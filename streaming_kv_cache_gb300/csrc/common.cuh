@@ -31,6 +31,7 @@ __device__ __forceinline__ int fastdiv(int n, int d, uint32_t m, int& rem) {
 struct Geom {
   int C, V, F, T, P, tail_cap, Hkv, d, row_cap, rope_len;
   uint32_t ft_m, t_m;   // fastdiv multipliers of F*T and T
+  int rope_steps;       // 1: table row = position, angles step along runs; 0: a table row per key
   __host__ __device__ int ring_rows() const { return V * F * T; }
   __host__ __device__ int n_visual() const { return P + V * F * T; }
 };
@@ -40,6 +41,7 @@ inline Geom geom_of(const skv_cache& c) {
   g.C = c.n_cache; g.V = c.n_view; g.F = c.n_frame; g.T = c.frame_len; g.P = c.prefix_len;
   g.tail_cap = c.tail_cap; g.Hkv = c.n_kv_head; g.d = c.head_dim; g.row_cap = c.row_cap;
   g.rope_len = c.rope_len;
+  g.rope_steps = c.rope_mode == 0;
   g.ft_m = fastdiv_m((uint32_t)(g.F * g.T > 0 ? g.F * g.T : 1));
   g.t_m = fastdiv_m((uint32_t)(g.T > 0 ? g.T : 1));
   return g;

@@ -180,4 +180,41 @@ cudaError_t launch_rope_table(float* tab, int n_pos, int d, double theta, cudaSt
   return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------------------
+// Multi-section rotary table: row n = the angles of the token at logical
+// index n.  A camera token tau of a frame whose first token is at b has the
+// position triple (b, b + tau / W, b + tau % W), every other token (n, n, n);
+// frequency i turns by the component its mask bits name.
+
+__global__ void mrope_table_kernel(float2* __restrict__ tab, int n_pos, int half, int d, double theta,
+                                   MRopeGeom m) {
+  const long long n_all = (long long)n_pos * half;
+  const long long vis_end = (long long)m.P + (long long)m.V * m.F * m.T;
+  for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < n_all;
+       e += (long long)gridDim.x * blockDim.x) {
+    const int n = (int)(e / half), i = (int)(e - (long long)n * half);
+    long long pt = n, ph = n, pw = n;
+    if (n >= m.P && n < vis_end) {
+      const int tau = (n - m.P) % m.T;
+      const long long b = n - tau;
+      pt = b;
+      ph = b + tau / m.W;
+      pw = b + tau % m.W;
+    }
+    const long long comp = ((m.h_mask >> i) & 1ull) ? ph : (((m.w_mask >> i) & 1ull) ? pw : pt);
+    const double inv_freq = pow(theta, -2.0 * i / d);
+    double s, c;
+    sincos((double)comp * inv_freq, &s, &c);
+    tab[e] = make_float2((float)c, (float)s);
+  }
+}
+
+cudaError_t launch_mrope_table(float* tab, int n_pos, int d, double theta, const MRopeGeom& m, cudaStream_t st) {
+  const long long n = (long long)n_pos * (d / 2);
+  const int blocks = (int)((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096);
+  mrope_table_kernel<<<blocks > 0 ? blocks : 1, 256, 0, st>>>(reinterpret_cast<float2*>(tab), n_pos, d / 2, d,
+                                                              theta, m);
+  return cudaGetLastError();
+}
+
 }  // namespace skv

@@ -19,6 +19,13 @@ cudaError_t launch_write_rows(const Geom& g, void* k, void* vt, const void* k_sr
 
 cudaError_t launch_rope_table(float* tab, int n_pos, int d, double theta, cudaStream_t st);
 
+// Geometry and frequency map of the multi-section rotary table.
+struct MRopeGeom {
+  int P, V, F, T, W;
+  uint64_t h_mask, w_mask;   // frequency i turns by h (bit i of h_mask), w (of w_mask), else t
+};
+cudaError_t launch_mrope_table(float* tab, int n_pos, int d, double theta, const MRopeGeom& m, cudaStream_t st);
+
 // The query tokens of one prefill launch, the same for every cache; a
 // cache's rows of q / out / lse hold NQ tokens.
 struct PrefillQuery {

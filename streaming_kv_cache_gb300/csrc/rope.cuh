@@ -33,18 +33,19 @@ __device__ __forceinline__ void rotate_pairs4(uint4& a, uint4& b, const float4 (
 
 // Logical position of physical key row r and how many rows from r on (r
 // included) continue with consecutive positions: the rest of the prefix, of
-// the ring frame, or the tail.
+// the ring frame, or the tail.  With a table row per key (rope_steps 0) the
+// run is always 1, so that every row reads its own angles.
 __device__ __forceinline__ void key_pos_run(const Geom& g, const int* __restrict__ heads, int r, int& pos,
                                             int& run) {
   const int u = r - g.P;
   if (u < 0) {
     pos = r;
-    run = g.P - r;
+    run = g.rope_steps ? g.P - r : 1;
     return;
   }
   if (u >= g.ring_rows()) {
     pos = r;
-    run = 1 << 30;
+    run = g.rope_steps ? 1 << 30 : 1;
     return;
   }
   const int FT = g.F * g.T;
@@ -54,7 +55,7 @@ __device__ __forceinline__ void key_pos_run(const Geom& g, const int* __restrict
   int f = sl - heads[v];
   if (f < 0) f += g.F;
   pos = g.P + v * FT + f * g.T + t;
-  run = g.T - t;
+  run = g.rope_steps ? g.T - t : 1;
 }
 
 // The (cos, sin) of the 8 frequencies of one chunk as packed fp32 pairs:

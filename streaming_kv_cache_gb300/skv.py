@@ -20,7 +20,7 @@ SKV_DEV_TIMEOUT, SKV_DEV_BAD_HEAD, SKV_DEV_TAIL_OVERFLOW, SKV_DEV_BAD_TAIL = 1, 
 
 # every function the C header declares
 EXPORTS = ("skv_version", "skv_status_string", "skv_last_cuda_error", "skv_row_cap",
-           "skv_build_rope_table", "kv_write_rows", "kv_stream_insert", "kv_stream_insert_noalloc",
+           "skv_build_rope_table", "skv_build_mrope_table", "kv_write_rows", "kv_stream_insert", "kv_stream_insert_noalloc",
            "stream_attn_prefill", "stream_attn_prefill_tail", "stream_attn_window",
            "skv_verify_workspace_bytes", "stream_attn_verify")
 
@@ -43,7 +43,8 @@ class skv_cache(ctypes.Structure):
                 ("k", ctypes.c_void_p), ("vt", ctypes.c_void_p),
                 ("head", ctypes.c_void_p), ("sync", ctypes.c_void_p),
                 ("rope", ctypes.c_void_p), ("status", ctypes.c_void_p),
-                ("wait_ns", ctypes.c_uint64)]
+                ("wait_ns", ctypes.c_uint64), ("rope_mode", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
 
 
 _lib_handle = None
@@ -65,6 +66,8 @@ def lib():
             "skv_last_cuda_error": ([], ctypes.c_int),
             "skv_row_cap": ([I32, I32, I32, I32, I32], I32),
             "skv_build_rope_table": ([P, I32, I32, ctypes.c_double, P], ctypes.c_int),
+            "skv_build_mrope_table": ([P, I32, I32, ctypes.c_double, I32, I32, I32, I32, I32,
+                                       ctypes.c_uint64, ctypes.c_uint64, P], ctypes.c_int),
             "kv_write_rows": ([cp, I32, I32, P, P, P], ctypes.c_int),
             "kv_stream_insert": ([cp, P, P, P], ctypes.c_int),
             "kv_stream_insert_noalloc": ([cp, P, P, P], ctypes.c_int),
@@ -129,6 +132,27 @@ def skv_build_rope_table(tab: torch.Tensor, theta: float):
            "skv_build_rope_table")
 
 
+def section_masks(sec) -> tuple:
+    """(h_mask, w_mask) of a frequency -> component map (0 = t, 1 = h, 2 = w)."""
+    h = sum(1 << i for i, c in enumerate(sec) if int(c) == 1)
+    w = sum(1 << i for i, c in enumerate(sec) if int(c) == 2)
+    return h, w
+
+
+def skv_build_mrope_table(tab: torch.Tensor, theta: float, P: int, V: int, F: int, T: int,
+                          grid_w: int, sec):
+    """The multi-section rotary table (see include/skv.h): row n holds the
+    angles of the token at logical index n; sec maps frequency i to its
+    component (0 = temporal, 1 = height, 2 = width)."""
+    n_pos, half, two = tab.shape
+    _need(tab, (n_pos, half, 2), torch.float32, "rope table")
+    if len(sec) != half:
+        raise ValueError("sec must give a component for each of the %d frequencies" % half)
+    h, w = section_masks(sec)
+    _check(lib().skv_build_mrope_table(_ptr(tab), n_pos, 2 * half, float(theta), P, V, F, T, grid_w,
+                                       h, w, _stream()), "skv_build_mrope_table")
+
+
 class StreamCache:
     """C independent streaming caches of one geometry, in device memory.
 
@@ -139,9 +163,14 @@ class StreamCache:
       sync   int32 [C][V]                insert counters
       rope   fp32 [rope_len][d/2][2]     (cos, sin) table
       status int32 [1]                   device status bits
+
+    mrope=(grid_w, sec) selects the multi-section rotary reading (rope_mode 1):
+    frames are rows of grid_w tokens and sec maps each of the d/2
+    frequencies to its component (0 = temporal, 1 = height, 2 = width).
     """
 
-    def __init__(self, C, P, V, F, T, Hkv, d, theta, tail_cap=128, device="cuda", wait_ns=0):
+    def __init__(self, C, P, V, F, T, Hkv, d, theta, tail_cap=128, device="cuda", wait_ns=0,
+                 mrope=None):
         self.C, self.P, self.V, self.F, self.T = C, P, V, F, T
         self.Hkv, self.d, self.theta, self.tail_cap = Hkv, d, float(theta), tail_cap
         self.row_cap = skv_row_cap(P, V, F, T, tail_cap)
@@ -154,8 +183,12 @@ class StreamCache:
         self.rope = torch.empty((self.rope_len, d // 2, 2), dtype=torch.float32, device=dev)
         self.status = torch.zeros((1,), dtype=torch.int32, device=dev)
         self.wait_ns = int(wait_ns)
+        self.rope_mode = 0 if mrope is None else 1
         with torch.cuda.device(dev):
-            skv_build_rope_table(self.rope, self.theta)
+            if mrope is None:
+                skv_build_rope_table(self.rope, self.theta)
+            else:
+                skv_build_mrope_table(self.rope, self.theta, P, V, F, T, mrope[0], mrope[1])
 
     @property
     def n_visual(self):
@@ -165,7 +198,7 @@ class StreamCache:
         return skv_cache(self.C, self.V, self.F, self.T, self.P, self.tail_cap, self.Hkv, self.d,
                          self.row_cap, self.rope_len, self.k.data_ptr(), self.vt.data_ptr(),
                          self.head.data_ptr(), self.sync.data_ptr(), self.rope.data_ptr(),
-                         self.status.data_ptr(), self.wait_ns)
+                         self.status.data_ptr(), self.wait_ns, self.rope_mode, 0)
 
     def device_status(self) -> int:
         return int(self.status.item())

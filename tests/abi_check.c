@@ -39,6 +39,8 @@ int main(void) {
   FIELD(rope);
   FIELD(status);
   FIELD(wait_ns);
+  FIELD(rope_mode);
+  FIELD(reserved);
 
   fails += expect("version", skv_version(), SKV_VERSION);
   fails += expect("row_cap", skv_row_cap(256, 4, 4, 180, 128), 3328);

@@ -66,12 +66,12 @@ def assert_lse(got: np.ndarray, want: np.ndarray, tol: float, what: str = "lse")
 class Pair:
     """A GPU StreamCache and oracle windows for a subset of its caches."""
 
-    def __init__(self, w: synth.Workload, tag: str, watch=None, tail_cap=None, wait_ns=0):
+    def __init__(self, w: synth.Workload, tag: str, watch=None, tail_cap=None, wait_ns=0, mrope=None):
         self.w, self.tag = w, tag
         self.watch = list(range(w.C)) if watch is None else list(watch)
         self.cache = skv.StreamCache(w.C, w.P, w.V, w.F, w.T, w.Hkv, w.d, w.theta,
                                      tail_cap=w.tail_cap if tail_cap is None else tail_cap,
-                                     wait_ns=wait_ns)
+                                     wait_ns=wait_ns, mrope=mrope)
         pk, pv = synth.prefix_kv(w, tag)
         if w.P:
             skv.kv_write_rows(self.cache, 0, to_dev(pk), to_dev(pv))

@@ -153,6 +153,23 @@ def test_tail_and_window_arguments(L):
     assert L.stream_attn_prefill_tail(ctypes.byref(bad), 32, 9, *t, p(FAKE), None, 1.0, None) == skv.SKV_ERR_INVALID
 
 
+def test_rope_mode_and_multi_section_table_arguments(L):
+    p = ctypes.c_void_p
+    bad = _desc(rope_mode=2)
+    assert L.stream_attn_prefill(ctypes.byref(bad), 32, p(FAKE), p(FAKE), None, 1.0, None) == skv.SKV_ERR_INVALID
+    ok = _desc(rope_mode=1)
+    assert L.stream_attn_prefill(ctypes.byref(ok), 32, p(FAKE), p(FAKE), None, 1.0, None) in (
+        skv.SKV_ERR_CUDA, skv.SKV_ERR_UNSUPPORTED)          # past every argument check
+    f = L.skv_build_mrope_table
+    assert f(p(FAKE), 10, 128, 1e6, 256, 4, 4, 180, 16, 0, 0, None) == skv.SKV_ERR_INVALID   # 180 % 16
+    assert f(p(FAKE), 10, 128, 1e6, 256, 4, 4, 180, 15, 3, 6, None) == skv.SKV_ERR_INVALID   # bit 1 in both
+    assert f(p(FAKE), 10, 256, 1e6, 256, 4, 4, 180, 15, 0, 0, None) == skv.SKV_ERR_INVALID   # d/2 > 64
+    assert f(None, 10, 128, 1e6, 256, 4, 4, 180, 15, 0, 0, None) == skv.SKV_ERR_INVALID
+    assert f(p(FAKE), 10, 128, 1e6, 256, 4, 4, 180, 15, 2, 4, None) in (skv.SKV_ERR_CUDA, skv.SKV_ERR_UNSUPPORTED)
+    h, w = skv.section_masks([0, 1, 2, 0, 1, 2, 0])
+    assert (h, w) == (0b0010010, 0b0100100)
+
+
 def test_rope_table_arguments(L):
     p = ctypes.c_void_p
     assert L.skv_build_rope_table(None, 10, 128, 1e4, None) == skv.SKV_ERR_INVALID
