@@ -7,6 +7,9 @@ One step = one pass of the whole path:
   3. stream_attn_verify   of a 9-token block on the Alpamayo-shaped cache
                           (prefix 256 + 4 x 4 x 180, 16 tail tokens), batch 64,
                           with the greedy accept-length reduction.
+After the step loop, kv_stream_insert alone is timed on rotating input sets
+that do not fit L2, and the one-kernel stream_attn_prefill_insert (steps 1
+and 2 fused) is timed beside it.
 
 The reported value is the prefill attention's algorithmic TFLOP/s over the
 whole step (unmasked query-key pairs only, 4*d FLOP each); the verify
@@ -395,6 +398,12 @@ def run_only(args):
         fn = lambda: skv.stream_attn_prefill_tail(cache, tail, q, kt, kt, w.sm_scale, out=out)
         work = tail_flop(w, n) / 1e12
         unit = "TFLOP/s"
+    elif args.only == "prefill_insert":
+        q = randn((w.C, w.n_new, w.Hq, w.d), w.q_scale)
+        out = torch.empty_like(q)
+        fn = lambda: skv.stream_attn_prefill_insert(cache, k_new, k_new, q, w.sm_scale, out=out)
+        work = prefill_flop(w) / 1e12
+        unit = "TFLOP/s"
     elif args.only == "insert":
         fn = lambda: skv.kv_stream_insert(cache, k_new, k_new)
         work = insert_bytes(w) / 1e9
@@ -448,7 +457,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["prefill", "verify", "insert", "window", "tail"], default=None,
+    ap.add_argument("--only", choices=["prefill", "prefill_insert", "verify", "insert", "window", "tail"],
+                    default=None,
                     help="profiling aid: time one kernel alone on a reduced case and print its ms")
     ap.add_argument("--layers", type=int, default=4,
                     help="layer caches (prefill/insert) or batch (verify) of the --only case")
@@ -586,6 +596,37 @@ def main():
 
     k_ms = {n: avg(n) for n in ev}
 
+    # --- the stand-alone frame insert: three input sets of 453 MB in turn,
+    # so that no call finds its inputs in L2 (the ring heads advance as in a
+    # step; the step's own inputs are the first set)
+    ins_in = [(k_new, v_new)] + [(randn(k_new.shape), randn(v_new.shape)) for _ in range(2)]
+    for i in range(3):
+        skv.kv_stream_insert(pc, *ins_in[i % 3])
+    torch.cuda.synchronize()
+    ins_ev = []
+    for i in range(12):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        skv.kv_stream_insert(pc, *ins_in[i % 3])
+        b.record()
+        ins_ev.append((a, b))
+    torch.cuda.synchronize()
+    ins_ms = statistics.mean(a.elapsed_time(b) for a, b in ins_ev)
+    # the insert and the prefill as one kernel (stream_attn_prefill_insert)
+    fz_ev = []
+    for i in range(8):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        skv.stream_attn_prefill_insert(pc, *ins_in[i % 3], q_new, pw.sm_scale, out=p_out)
+        b.record()
+        if i >= 2:
+            fz_ev.append((a, b))
+    torch.cuda.synchronize()
+    fz_ms = statistics.mean(a.elapsed_time(b) for a, b in fz_ev)
+    del ins_in
+    if pc.device_status():
+        raise RuntimeError("device status %d in the insert timing" % pc.device_status())
+
     # --- end to end through host buffers (pinned), same step, same metric
     h_k = k_new.cpu().pin_memory(); h_v = v_new.cpu().pin_memory(); h_q = q_new.cpu().pin_memory()
     h_qb = q_blk.cpu().pin_memory(); h_kb = k_blk.cpu().pin_memory(); h_vb = v_blk.cpu().pin_memory()
@@ -687,7 +728,7 @@ def main():
     pk, src = peaks()
     pre_tf = flop / (k_ms["prefill"] * 1e-3) / 1e12
     ver_gbs = verify_bytes(vw) / (k_ms["verify"] * 1e-3) / 1e9
-    ins_gbs = insert_bytes(pw) / (k_ms["insert"] * 1e-3) / 1e9
+    ins_gbs = insert_bytes(pw) / (ins_ms * 1e-3) / 1e9
     tag = "of measured" if src == "measured" else "of fallback"
 
     cpu = None
@@ -712,9 +753,15 @@ def main():
                                 "peak": pk["hbm_gbs"], "unit": "GB/s",
                                 "frac": ver_gbs / pk["hbm_gbs"], "peak_source": tag,
                                 "traffic": traffic_for("verify_tc.cu")},
-            "insert_roofline": {"bound": "hbm", "kernel": "kv_stream_insert", "achieved": ins_gbs,
+            "insert_roofline": {"bound": "hbm", "kernel": "kv_stream_insert (stand-alone)", "achieved": ins_gbs,
                                 "peak": pk["hbm_gbs"], "unit": "GB/s",
-                                "frac": ins_gbs / pk["hbm_gbs"], "peak_source": tag},
+                                "frac": ins_gbs / pk["hbm_gbs"], "peak_source": tag,
+                                "ms": ins_ms, "inputs": "3 rotating input sets of 453 MB each, "
+                                                        "larger than L2"},
+            "fused_prefill_insert": {"ms": fz_ms, "tflops": flop / (fz_ms * 1e-3) / 1e12,
+                                     "vs_insert_plus_prefill_ms": k_ms["insert"] + k_ms["prefill"],
+                                     "note": "insert and prefill as one kernel, same results bit for bit; "
+                                             "not used in the step because it is slower"},
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / args.steps,

@@ -254,6 +254,29 @@ int stream_attn_prefill(const skv_cache* cache, int32_t n_q_head, const void* q_
                         float* lse, float sm_scale, void* stream);
 
 /*
+ * stream_attn_prefill_insert -- kv_stream_insert of the step's new frames
+ * followed by stream_attn_prefill of their queries, as one call (blog
+ * section 3.1: each step evicts the oldest frame and prefills only the
+ * newest; the insert is folded into the prefill so that the new frames are
+ * read from the input once, by the attention kernel itself).  Same inputs,
+ * results and status bits as the two calls: the ring holds the new frames
+ * bit for bit and the heads are advanced afterwards.
+ *
+ * k_new, v_new: device bf16 [C][V][T][Hkv][d] (as kv_stream_insert);
+ * q_new, out, lse as stream_attn_prefill.  cache->sync is needed (zeroed
+ * counters, left at 0).
+ *
+ * With head_dim 128 and P and T multiples of 64 it is one kernel launch: the
+ * new frames' K/V tiles come straight from k_new / v_new, the CTA pair of
+ * each view's last query block writes that frame into the ring slot of the
+ * oldest frame, and the last CTA of a cache to start advances its heads.
+ * Otherwise the call enqueues the insert and then the prefill.
+ */
+int stream_attn_prefill_insert(const skv_cache* cache, int32_t n_q_head, const void* k_new,
+                               const void* v_new, const void* q_new, void* out, float* lse,
+                               float sm_scale, void* stream);
+
+/*
  * stream_attn_prefill_tail -- the trajectory / text tokens that follow the
  * views, as queries (blog section 3.2: they see every view and are causal
  * among themselves; with the newest frames they are a step's only new

@@ -9,5 +9,6 @@ from . import synth  # noqa: F401
 from .skv import (EXPORTS, SkvError, StreamCache, kv_stream_insert,  # noqa: F401
                   kv_stream_insert_noalloc, kv_write_rows,
                   lib, skv_build_rope_table, skv_row_cap, skv_verify_workspace_bytes,
-                  status_string, stream_attn_prefill, stream_attn_prefill_tail, stream_attn_verify,
+                  skv_build_mrope_table, status_string, stream_attn_prefill,
+                  stream_attn_prefill_insert, stream_attn_prefill_tail, stream_attn_verify,
                   stream_attn_window, verify_workspace)

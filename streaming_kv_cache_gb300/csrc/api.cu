@@ -208,6 +208,41 @@ int stream_attn_prefill(const skv_cache* cache, int32_t n_q_head, const void* q_
   return e == cudaSuccess ? SKV_OK : cuda_fail(e);
 }
 
+int stream_attn_prefill_insert(const skv_cache* cache, int32_t n_q_head, const void* k_new,
+                               const void* v_new, const void* q_new, void* out, float* lse,
+                               float sm_scale, void* stream) {
+  int rc = check_cache(cache);
+  if (rc) return rc;
+  if ((rc = check_sync(cache))) return rc;
+  if (n_q_head < 1 || n_q_head % cache->n_kv_head) return SKV_ERR_INVALID;
+  if (128 % (n_q_head / cache->n_kv_head)) return SKV_ERR_UNSUPPORTED;
+  if ((rc = check_prefill_shape(cache, (long long)cache->n_view * cache->frame_len, n_q_head))) return rc;
+  if (!(sm_scale > 0.f) || sm_scale != sm_scale) return SKV_ERR_INVALID;
+  if (cache->n_cache == 0) return SKV_OK;
+  if (!k_new || !v_new || !q_new || !out) return SKV_ERR_INVALID;
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(q_new) || !aligned16(out)) return SKV_ERR_INVALID;
+  if (lse && ((uintptr_t)lse & 3u)) return SKV_ERR_INVALID;
+  if ((rc = check_device())) return rc;
+  const skv::Geom g = skv::geom_of(*cache);
+  cudaStream_t st = (cudaStream_t)stream;
+  skv::PrefillQuery qs{};
+  qs.nf = 1;
+  qs.NQ = g.V * g.T;
+  cudaError_t e;
+  if (skv::prefill_insert_fusable(g)) {
+    e = skv::launch_prefill_tc(g, n_q_head, qs, q_new, out, lse, cache->k, cache->vt, cache->rope, cache->head,
+                               sm_scale, cache->status, cache->wait_ns, st, k_new, v_new, cache->sync);
+  } else {
+    // the two steps one after the other on the stream
+    e = skv::launch_write_rows(g, cache->k, cache->vt, k_new, v_new, g.V, g.T, 1, 0, cache->head, cache->sync,
+                               nullptr, cache->status, st);
+    if (e == cudaSuccess)
+      e = skv::launch_prefill_tc(g, n_q_head, qs, q_new, out, lse, cache->k, cache->vt, cache->rope, cache->head,
+                                 sm_scale, cache->status, cache->wait_ns, st);
+  }
+  return e == cudaSuccess ? SKV_OK : cuda_fail(e);
+}
+
 int stream_attn_prefill_tail(const skv_cache* cache, int32_t n_q_head, int32_t n_tok,
                              const int32_t* tail_len, const void* q_tail, const void* k_tail,
                              const void* v_tail, void* out, float* lse, float sm_scale,

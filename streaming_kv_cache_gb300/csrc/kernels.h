@@ -39,9 +39,14 @@ struct PrefillQuery {
   int q_tail0;              // token of the first tail query; prefix token j at j
 };
 
+// With k_new / v_new ([C][V][T][Hkv][d]) and sync given, the launch also does
+// the frame insert (new-frame queries only; prefill_insert_fusable geometry):
+// heads still name the oldest frames when it starts and are advanced by it.
 cudaError_t launch_prefill_tc(const Geom& g, int Hq, const PrefillQuery& qs, const void* q, void* out, float* lse,
-                              const void* k, const void* vt, const float* rope, const int32_t* head,
-                              float sm_scale, int32_t* status, uint64_t wait_ns, cudaStream_t st);
+                              const void* k, const void* vt, const float* rope, int32_t* head,
+                              float sm_scale, int32_t* status, uint64_t wait_ns, cudaStream_t st,
+                              const void* k_new = nullptr, const void* v_new = nullptr, int32_t* sync = nullptr);
+bool prefill_insert_fusable(const Geom& g);
 
 cudaError_t launch_verify_tc(const Geom& g, int Hq, int blk, const int32_t* tail_len, const void* q, void* out,
                              const void* k, const void* vt, const float* rope, const int32_t* head,

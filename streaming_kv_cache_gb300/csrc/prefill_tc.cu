@@ -90,7 +90,10 @@ struct Layout {
   // per softmax row: the second run of its mask (a2, n2), its output row
   // (-1: none) and its LSE index
   static constexpr int MASK_OFF = TILE_OFF + MAX_TILES * 4;
-  static constexpr int BYTES = MASK_OFF + 4 * 2 * BM * 4;
+  // per tile, with the insert fused: bit b set = rows [r0 + 64b, r0 + 64b + 64)
+  // are a new frame, read from the step's input instead of the ring
+  static constexpr int SRC_OFF = MASK_OFF + 4 * 2 * BM * 4;
+  static constexpr int BYTES = SRC_OFF + MAX_TILES;
   static constexpr int ALLOC = BYTES + 1024;   // slack for 1024-byte alignment
 };
 
@@ -133,6 +136,14 @@ struct PrefillParams {
   int32_t* status;
   float scale_log2;
   uint64_t wait_ns;
+  // the insert fused into the new-frame prefill: the ring heads still name
+  // the oldest frames, each view's new frame is read from the step's input
+  // and written into that slot by the CTA pair of its last query block, and
+  // the last CTA of a cache to start advances the heads (counter in sync)
+  int32_t* head_w;        // heads to advance (fused only)
+  int32_t* sync;          // [C][V] zeroed counters; [c][0] counts the CTAs of cache c
+  uint16_t* ring_k;       // the cache's k and vt, written with the new frames
+  uint16_t* ring_vt;
 };
 
 // SW: compiled for a wait limit under the suspend hint (see tc::bounded_wait)
@@ -152,10 +163,13 @@ __device__ __forceinline__ void ring_hole(const Geom& g, int v, int f, int slot,
   a2 = base;
 }
 
-template <int D, bool SW>
+// FUSED: the frame insert is done by this launch (see PrefillParams): the new
+// frames' K and V come from the step's input through tmap_kn / tmap_vn.
+template <int D, bool SW, bool FUSED>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
-                  const __grid_constant__ CUtensorMap tmap_q, const PrefillParams p) {
+                  const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_kn,
+                  const __grid_constant__ CUtensorMap tmap_vn, const PrefillParams p) {
   using L = Layout<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -168,6 +182,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
   int* s_head = reinterpret_cast<int*>(smem + L::HEAD_OFF);
   int* s_mask = reinterpret_cast<int*>(smem + L::MASK_OFF);
   int* s_wrap = reinterpret_cast<int*>(smem + L::MISC_OFF + 12);   // 1: some row's mask has a second run
+  uint8_t* s_src = smem + L::SRC_OFF;
 
   const Geom& g = p.g;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -232,13 +247,15 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
       *s_abort = 0;
     }
     // ring heads of the views whose rows the item reads, one lane per view
+    // (with the insert fused: the heads as they are once it is done)
     bool ok = bad == 0;
     for (int v = lane; v <= vmax; v += 32) {
       const int hv = head_c[v];
       ok = ok && hv >= 0 && hv < g.F;
-      s_head[v] = hv;
+      s_head[v] = FUSED ? (hv + 1) % g.F : hv;
     }
     ok = __all_sync(0xffffffffu, ok);
+    __syncwarp();
     // tile list over physical key rows [0, row_end), skipping tiles made only
     // of ring rows that no query of the pair may see (the hole of its last
     // token lies inside every other token's); 32 tiles per step
@@ -246,7 +263,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
     if (ok) {
       int a1 = 0, n1 = 0, a2 = 0, n2 = 0;
       if (vq >= 0) {
-        const int slot = (head_c[vq] + fq) % g.F;
+        const int slot = (s_head[vq] + fq) % g.F;
         ring_hole(g, vq, fq, slot, t_max, a1, n1, a2, n2);
         // the first token's hole holds every other token's: if it has no
         // second run, no row's mask has one
@@ -259,7 +276,25 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
         const int k = k0 + lane, r0 = k * BN, r1 = min(r0 + BN, row_end);
         const bool keep = k < n_all && !(r0 >= a1 && r1 <= a1 + n1) && !(r0 >= a2 && r1 <= a2 + n2);
         const uint32_t ball = __ballot_sync(0xffffffffu, keep);
-        if (keep) s_tiles[n + __popc(ball & ((1u << lane) - 1))] = r0;
+        if (keep) {
+          const int slot_j = n + __popc(ball & ((1u << lane) - 1));
+          s_tiles[slot_j] = r0;
+          if (FUSED) {
+            // which 64-row block of the tile is a view's new frame (bits 0-1),
+            // and which of those this pair writes into the ring (bits 2-3): the
+            // pair of a view's last query block sees all of its new frame
+            uint32_t f = 0;
+            for (int b = 0; b < 2; ++b) {
+              const int u = r0 + 64 * b - g.P;
+              if (u < 0 || u >= g.ring_rows() || r0 + 64 * b >= row_end) continue;
+              const int v = u / FT, sl = (u % FT) / g.T;
+              if (sl != (s_head[v] + g.F - 1) % g.F) continue;
+              f |= 1u << b;
+              if (v == vq && pc == p.nbf - 1) f |= 4u << b;
+            }
+            s_src[slot_j] = (uint8_t)f;
+          }
+        }
         n += __popc(ball);
       }
     } else if (rank == 0 && lane == 0) {
@@ -281,6 +316,21 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
   tc::tc_fence_after();
   const uint32_t tmem = *s_tmem;
   const int nt = *s_ntiles;
+  if (FUSED && tid == 0) {
+    // every CTA of the cache reads the heads in its set-up, before this
+    // arrival; the last to arrive advances them (a head out of range stays,
+    // as the insert leaves it) and leaves the counter at zero
+    __threadfence();
+    const int per_cache = 2 * g.Hkv * p.items;
+    if (atomicAdd(p.sync + (size_t)c * g.V, 1) == per_cache - 1) {
+      for (int v = 0; v < g.V; ++v) {
+        const int hv = p.head_w[(size_t)c * g.V + v];
+        if (hv >= 0 && hv < g.F) p.head_w[(size_t)c * g.V + v] = (hv + 1) % g.F;
+      }
+      p.sync[(size_t)c * g.V] = 0;
+      __threadfence();
+    }
+  }
 
   if (warp >= 8 && warp < WARP_ROPE) {
     tc::setmaxnreg_dec<REG_CTRL>();
@@ -306,18 +356,44 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
           if (j >= NST &&
               !tc::mbar_wait_cluster<SW>(bar((is_k ? B_KEMPTY : B_VEMPTY) + s), (u - 1) & 1, wait_ns, s_abort))
             break;
+          // a 64-row block of a view's new frame comes from the step's input
+          // [C][V][T][Hkv][d]: K rows as they are, V token-major (an MN-major
+          // operand for the PV product); every other block from the ring
+          const uint32_t src = FUSED ? s_src[j] : 0u;
+          auto new_block = [&](int r, int& t_in, int& cv) {
+            const int u = r - g.P, v = u / FT;
+            t_in = u % FT % g.T;
+            cv = c * g.V + v;
+          };
           if (is_k) {
             tc::mbar_arrive_expect_tx(bar(B_KFULL + s), L::KST);
+            if (FUSED && (src >> rank) & 1u) {
+              int t_in, cv;
+              new_block(r0 + HN * (int)rank, t_in, cv);
 #pragma unroll
-            for (int hf = 0; hf < D / 64; ++hf)
-              tc::tma_load_3d(sbase + L::K_OFF + s * L::KST + hf * L::HALF_K, &tmap_k, bar(B_KFULL + s), hf * 64,
-                              r0 + HN * (int)rank, zc);
+              for (int hf = 0; hf < D / 64; ++hf)
+                tc::tma_load_4d(sbase + L::K_OFF + s * L::KST + hf * L::HALF_K, &tmap_kn, bar(B_KFULL + s), hf * 64,
+                                h, t_in, cv);
+            } else {
+#pragma unroll
+              for (int hf = 0; hf < D / 64; ++hf)
+                tc::tma_load_3d(sbase + L::K_OFF + s * L::KST + hf * L::HALF_K, &tmap_k, bar(B_KFULL + s), hf * 64,
+                                r0 + HN * (int)rank, zc);
+            }
           } else {
             tc::mbar_arrive_expect_tx(bar(B_VFULL + s), L::VST);
 #pragma unroll
-            for (int kh = 0; kh < 2; ++kh)
-              tc::tma_load_3d(sbase + L::V_OFF + s * L::VST + kh * L::HALF_V, &tmap_v, bar(B_VFULL + s),
-                              r0 + kh * 64, (D / 2) * (int)rank, zc);
+            for (int kh = 0; kh < 2; ++kh) {
+              if (FUSED && (src >> kh) & 1u) {
+                int t_in, cv;
+                new_block(r0 + kh * 64, t_in, cv);
+                tc::tma_load_4d(sbase + L::V_OFF + s * L::VST + kh * L::HALF_V, &tmap_vn, bar(B_VFULL + s),
+                                (D / 2) * (int)rank, h, t_in, cv);
+              } else {
+                tc::tma_load_3d(sbase + L::V_OFF + s * L::VST + kh * L::HALF_V, &tmap_v, bar(B_VFULL + s),
+                                r0 + kh * 64, (D / 2) * (int)rank, zc);
+              }
+            }
           }
           issued = j + 1;
         }
@@ -336,15 +412,48 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
     } else if (warp == WARP_VFWD) {
       // ------------------- tell the even CTA when this CTA's V^T half landed
       // (one barrier per stage with the K rotation: a key tile is ready for
-      // both of its MMAs at once, so the MMA issuer waits once per tile)
-      if (lane == 0 && nt > 0) {
+      // both of its MMAs at once, so the MMA issuer waits once per tile).
+      // With the insert fused, a new-frame block this pair writes into the
+      // ring (token-major in shared memory) goes out transposed first.
+      if (nt > 0) {
         for (int j = 0; j < nt; ++j) {
           const int s = j % NST, u = j / NST;
-          if (!tc::mbar_wait<SW>(bar(B_VFULL + s), u & 1, wait_ns, s_abort)) {
-            set_status(p.status, SKV_DEV_TIMEOUT);
+          const bool ok = __all_sync(0xffffffffu, tc::mbar_wait<SW>(bar(B_VFULL + s), u & 1, wait_ns, s_abort));
+          if (!ok) {
+            if (lane == 0) set_status(p.status, SKV_DEV_TIMEOUT);
             break;
           }
-          tc::mbar_arrive_cluster_cta_if(bar_even(B_KROT + s), true);
+          if (FUSED) {
+            const uint32_t src = s_src[j];
+#pragma unroll 1
+            for (int kh = 0; kh < 2; ++kh) {
+              if (!((src >> (2 + kh)) & 1u)) continue;
+              // 64 keys x 64 dimensions, one key per 128-byte swizzled row;
+              // lane: dimensions lane and lane + 32, 8 keys per 16-byte store
+              const uint8_t* box = smem + L::V_OFF + s * L::VST + kh * L::HALF_V;
+              uint16_t* dst = p.ring_vt + ((size_t)zc * D + (D / 2) * rank) * g.row_cap + s_tiles[j] + 64 * kh;
+#pragma unroll
+              for (int dh = 0; dh < 2; ++dh) {
+                const int dd = lane + 32 * dh;
+#pragma unroll 1
+                for (int i = 0; i < 8; ++i) {
+                  uint32_t w[4];
+#pragma unroll
+                  for (int e = 0; e < 8; e += 2) {
+                    const int k0 = 8 * i + e;
+                    const uint16_t lo = *reinterpret_cast<const uint16_t*>(
+                        box + k0 * 128 + (((dd >> 3) ^ (k0 & 7)) << 4) + (dd & 7) * 2);
+                    const uint16_t hi = *reinterpret_cast<const uint16_t*>(
+                        box + (k0 + 1) * 128 + (((dd >> 3) ^ ((k0 + 1) & 7)) << 4) + (dd & 7) * 2);
+                    w[e / 2] = (uint32_t)lo | ((uint32_t)hi << 16);
+                  }
+                  *reinterpret_cast<uint4*>(dst + (size_t)dd * g.row_cap + 8 * i) = make_uint4(w[0], w[1], w[2], w[3]);
+                }
+              }
+            }
+            __syncwarp();
+          }
+          tc::mbar_arrive_cluster_cta_if(bar_even(B_KROT + s), lane == 0);
         }
       }
     } else if (warp == WARP_MMA) {
@@ -352,6 +461,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
       if (lane == 0 && nt > 0 && rank == 0) {
         constexpr uint32_t idesc_qk = tc::idesc_f16(2 * BM, BN);
         constexpr uint32_t idesc_pv = tc::idesc_bf16(2 * BM, D);
+        constexpr uint32_t idesc_pv_mn = tc::idesc_bf16_bmn(2 * BM, D);
         // descriptors advance by adding (byte offset >> 4) to the start-address field;
         // each CTA's operands sit at the same offsets in its own shared memory.
         // The k-steps are unrolled (one thread must stay ahead of the tensor
@@ -371,12 +481,16 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
             tc::mma_ss_pair(tmem + i * 128, dq + oq, dk + ok, idesc_qk, kk > 0);
           }
         };
-        auto issue_pv = [&](int i, int s, bool acc) {
+        // mn: bit kh set = key block kh of the tile holds token-major values
+        // (a new frame read from the step's input), an MN-major operand: 8
+        // keys of 128 bytes per 1024-byte group, 16 keys = 2048 bytes per k-step
+        auto issue_pv = [&](int i, int s, bool acc, uint32_t mn) {
           const uint64_t dv = tc::opaque(dv0 + ((uint32_t)(s * L::VST) >> 4));
 #pragma unroll
           for (int kk = 0; kk < BN / 16; ++kk) {
-            const uint32_t ov = ((kk >> 2) * L::HALF_V + (kk & 3) * 32) >> 4;
-            tc::mma_ts_pair(tmem + 256 + i * 128, tmem + i * 128 + kk * 8, dv + ov, idesc_pv,
+            const bool bmn = FUSED && ((mn >> (kk >> 2)) & 1u);
+            const uint32_t ov = ((kk >> 2) * L::HALF_V + (kk & 3) * (bmn ? 2048 : 32)) >> 4;
+            tc::mma_ts_pair(tmem + 256 + i * 128, tmem + i * 128 + kk * 8, dv + ov, bmn ? idesc_pv_mn : idesc_pv,
                             (acc || kk > 0) ? 1u : 0u);
           }
         };
@@ -395,7 +509,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
           const int s2 = (j + 1) % NST, u2 = (j + 1) / NST;
           if (!(ok = tc::mbar_wait_short<SW>(bar(B_PFULL), j & 1, wait_ns, s_abort))) break;
           tc::tc_fence_after();
-          issue_pv(0, s, j > 0);
+          const uint32_t mn = FUSED ? (uint32_t)s_src[j] & 3u : 0u;
+          issue_pv(0, s, j > 0, mn);
           tc::mma_commit_pair(bar(B_ODONE));
           if (j + 1 < nt) {
             if (!(ok = tc::mbar_wait_short<SW>(bar(B_KROT + s2), u2 & 1, wait_ns, s_abort))) break;
@@ -405,7 +520,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
           }
           if (!(ok = tc::mbar_wait_short<SW>(bar(B_PFULL + 1), j & 1, wait_ns, s_abort))) break;
           tc::tc_fence_after();
-          issue_pv(1, s, j > 0);
+          issue_pv(1, s, j > 0, mn);
           tc::mma_commit_pair(bar(B_ODONE + 1));
           tc::mma_commit_pair(bar(B_VEMPTY + s));
           if (j + 1 < nt) {
@@ -464,7 +579,24 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
 #pragma unroll 1
     for (int j = 0; j < nt; ++j) {
       const int s = j % NST, u = j / NST;
-      if (!tc::mbar_wait<SW>(bar(B_KFULL + s), u & 1, wait_ns, s_abort)) {
+      bool ok = tc::mbar_wait<SW>(bar(B_KFULL + s), u & 1, wait_ns, s_abort);
+      const uint32_t src = FUSED ? (uint32_t)s_src[j] : 0u;
+      if (FUSED && ((src >> (2 + rank)) & 1u)) {
+        // this CTA's K block is a new frame of the pair's own view: it goes
+        // into the ring slot of the oldest frame (pre-RoPE, by TMA) before it
+        // is rotated in place.  (Barriers here see all four RoPE warps take
+        // the same path: the predicate is the AND of every thread's wait.)
+        ok = tc::bar_and(3, 128, ok);
+        if (ok && rt == 0) {
+#pragma unroll
+          for (int hf = 0; hf < D / 64; ++hf)
+            tc::tma_store_3d(&tmap_k, sbase + L::K_OFF + s * L::KST + hf * L::HALF_K, hf * 64,
+                             s_tiles[j] + HN * (int)rank, zc);
+          tc::tma_store_commit_wait_read();
+        }
+        tc::bar_and(3, 128, true);
+      }
+      if (!ok) {
         set_status(p.status, SKV_DEV_TIMEOUT);
         break;
       }
@@ -707,7 +839,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
 // largest carve-out made the 36-layer call 3% slower).
 template <typename K>
 cudaError_t set_smem_once(K kernel, int bytes, int variant) {
-  static std::atomic<int> done[64][4];
+  static std::atomic<int> done[64][6];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -769,10 +901,16 @@ cudaError_t make_kv_tmaps(const Geom& g, const void* k, const void* vt, int k_bo
   return cudaSuccess;
 }
 
+bool prefill_insert_fusable(const Geom& g) { return g.d == 128 && g.P % 64 == 0 && g.T % 64 == 0; }
+
 cudaError_t launch_prefill_tc(const Geom& g, int Hq, const PrefillQuery& qs, const void* q, void* out, float* lse,
-                              const void* k, const void* vt, const float* rope, const int32_t* head,
-                              float sm_scale, int32_t* status, uint64_t wait_ns, cudaStream_t st) {
+                              const void* k, const void* vt, const float* rope, int32_t* head,
+                              float sm_scale, int32_t* status, uint64_t wait_ns, cudaStream_t st,
+                              const void* k_new, const void* v_new, int32_t* sync) {
   if ((g.row_cap + BN - 1) / BN > MAX_TILES || g.V > MAX_VIEWS) return cudaErrorNotSupported;
+  const bool fused = k_new != nullptr;
+  if (fused && (!prefill_insert_fusable(g) || qs.nf != 1 || qs.n_tail || qs.prefix || !v_new || !sync))
+    return cudaErrorInvalidValue;
   // output rows (token, head) and LSE entries are indexed in 32 bits
   if ((long long)g.C * qs.NQ * Hq > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
   CUtensorMap tk, tv, tq;
@@ -792,6 +930,22 @@ cudaError_t launch_prefill_tc(const Geom& g, int Hq, const PrefillQuery& qs, con
            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
+  }
+  // the step's new frames [C][V][T][Hkv][d]: boxes of 64 columns x 64 tokens
+  // of one (cache, view, kv head), as the ring's K boxes and as token-major V
+  CUtensorMap tkn = tk, tvn = tv;
+  if (fused) {
+    auto fn = tmap_encode_fn();
+    if (!fn) return cudaErrorNotSupported;
+    cuuint64_t dims[4] = {(cuuint64_t)g.d, (cuuint64_t)g.Hkv, (cuuint64_t)g.T, (cuuint64_t)g.C * g.V};
+    cuuint64_t strides[3] = {(cuuint64_t)g.d * 2, (cuuint64_t)g.Hkv * g.d * 2, (cuuint64_t)g.T * g.Hkv * g.d * 2};
+    cuuint32_t box[4] = {64, 1, 64, 1};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    for (int i = 0; i < 2; ++i)
+      if (fn(i ? &tvn : &tkn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(i ? v_new : k_new), dims,
+             strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
   }
   PrefillParams p;
   p.g = g;
@@ -814,6 +968,10 @@ cudaError_t launch_prefill_tc(const Geom& g, int Hq, const PrefillQuery& qs, con
   p.lse = lse;
   p.rope = reinterpret_cast<const float2*>(rope);
   p.head = head;
+  p.head_w = head;
+  p.sync = sync;
+  p.ring_k = static_cast<uint16_t*>(const_cast<void*>(k));
+  p.ring_vt = static_cast<uint16_t*>(const_cast<void*>(vt));
   p.status = status;
   p.scale_log2 = sm_scale * 1.4426950408889634f;
   p.wait_ns = wait_ns ? wait_ns : 2000000000ull;
@@ -825,15 +983,18 @@ cudaError_t launch_prefill_tc(const Geom& g, int Hq, const PrefillQuery& qs, con
   auto launch = [&](auto kernel, int smem, int variant) -> cudaError_t {
     cudaError_t err = set_smem_once(kernel, smem, variant);
     if (err != cudaSuccess) return err;
-    kernel<<<(unsigned)blocks, NTHREADS, smem, st>>>(tk, tv, tq, p);
+    kernel<<<(unsigned)blocks, NTHREADS, smem, st>>>(tk, tv, tq, tkn, tvn, p);
     return cudaSuccess;
   };
-  if (g.d == 128)
-    e = sw ? launch(prefill_tc_kernel<128, true>, Layout<128>::ALLOC, 2)
-           : launch(prefill_tc_kernel<128, false>, Layout<128>::ALLOC, 0);
+  if (fused)
+    e = sw ? launch(prefill_tc_kernel<128, true, true>, Layout<128>::ALLOC, 5)
+           : launch(prefill_tc_kernel<128, false, true>, Layout<128>::ALLOC, 4);
+  else if (g.d == 128)
+    e = sw ? launch(prefill_tc_kernel<128, true, false>, Layout<128>::ALLOC, 2)
+           : launch(prefill_tc_kernel<128, false, false>, Layout<128>::ALLOC, 0);
   else
-    e = sw ? launch(prefill_tc_kernel<64, true>, Layout<64>::ALLOC, 3)
-           : launch(prefill_tc_kernel<64, false>, Layout<64>::ALLOC, 1);
+    e = sw ? launch(prefill_tc_kernel<64, true, false>, Layout<64>::ALLOC, 3)
+           : launch(prefill_tc_kernel<64, false, false>, Layout<64>::ALLOC, 1);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

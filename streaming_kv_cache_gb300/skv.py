@@ -21,7 +21,8 @@ SKV_DEV_TIMEOUT, SKV_DEV_BAD_HEAD, SKV_DEV_TAIL_OVERFLOW, SKV_DEV_BAD_TAIL = 1, 
 # every function the C header declares
 EXPORTS = ("skv_version", "skv_status_string", "skv_last_cuda_error", "skv_row_cap",
            "skv_build_rope_table", "skv_build_mrope_table", "kv_write_rows", "kv_stream_insert", "kv_stream_insert_noalloc",
-           "stream_attn_prefill", "stream_attn_prefill_tail", "stream_attn_window",
+           "stream_attn_prefill", "stream_attn_prefill_insert", "stream_attn_prefill_tail",
+           "stream_attn_window",
            "skv_verify_workspace_bytes", "stream_attn_verify")
 
 
@@ -72,6 +73,7 @@ def lib():
             "kv_stream_insert": ([cp, P, P, P], ctypes.c_int),
             "kv_stream_insert_noalloc": ([cp, P, P, P], ctypes.c_int),
             "stream_attn_prefill": ([cp, I32, P, P, P, ctypes.c_float, P], ctypes.c_int),
+            "stream_attn_prefill_insert": ([cp, I32, P, P, P, P, P, ctypes.c_float, P], ctypes.c_int),
             "stream_attn_prefill_tail": ([cp, I32, I32, P, P, P, P, P, P, ctypes.c_float, P],
                                          ctypes.c_int),
             "stream_attn_window": ([cp, I32, P, P, P, ctypes.c_float, P], ctypes.c_int),
@@ -253,6 +255,28 @@ def stream_attn_prefill(cache: StreamCache, q_new: torch.Tensor, sm_scale: float
     dd = cache.desc()
     _check(lib().stream_attn_prefill(ctypes.byref(dd), Hq, _ptr(q_new), _ptr(out), _ptr(lse),
                                      float(sm_scale), _stream()), "stream_attn_prefill")
+    return (out, lse) if lse is not None else out
+
+
+def stream_attn_prefill_insert(cache: StreamCache, k_new: torch.Tensor, v_new: torch.Tensor,
+                               q_new: torch.Tensor, sm_scale: float, out: torch.Tensor | None = None,
+                               lse: torch.Tensor | bool | None = None):
+    """kv_stream_insert(k_new, v_new) then stream_attn_prefill(q_new) as one
+    call (one kernel where the geometry allows).  Returns out (and lse when
+    asked for)."""
+    shp = (cache.C, cache.V, cache.T, cache.Hkv, cache.d)
+    _need(k_new, shp, torch.bfloat16, "k_new")
+    _need(v_new, shp, torch.bfloat16, "v_new")
+    C, nq, Hq, d = q_new.shape
+    _need(q_new, (cache.C, cache.V * cache.T, Hq, cache.d), torch.bfloat16, "q_new")
+    if out is None:
+        out = torch.empty_like(q_new)
+    _need(out, q_new.shape, torch.bfloat16, "out")
+    lse = _lse_arg(lse, C, Hq, nq, q_new.device)
+    dd = cache.desc()
+    _check(lib().stream_attn_prefill_insert(ctypes.byref(dd), Hq, _ptr(k_new), _ptr(v_new), _ptr(q_new),
+                                            _ptr(out), _ptr(lse), float(sm_scale), _stream()),
+           "stream_attn_prefill_insert")
     return (out, lse) if lse is not None else out
 
 
