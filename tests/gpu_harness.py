@@ -13,6 +13,13 @@ from streaming_kv_cache_gb300 import skv, synth
 # tolerance stated for the attention outputs (bf16 in, fp32 accumulate)
 MAX_ABS = 1e-2
 MEAN_ABS = 1e-3
+# LSE (natural log) bound, set from the measured errors: the largest seen by
+# any parity test on N(0,1)-scaled inputs is 7.9e-4 (the whole window of the
+# 8-heads-per-kv-head geometry; the five workloads stay under 5e-4), and the
+# bound keeps a margin of about 4x over it.  Tests whose scores are k times
+# larger by construction scale it by k (the fp16 rounding of the rotated
+# operands moves a score in proportion to its size).
+LSE_TOL = 3e-3
 
 
 def to_dev(bits: np.ndarray) -> torch.Tensor:

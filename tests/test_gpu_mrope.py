@@ -9,12 +9,11 @@ import torch
 from oracle import skv_oracle as O
 from streaming_kv_cache_gb300 import skv, synth
 
-from gpu_harness import Pair, assert_close, assert_lse, bf16_dev_to_f64, to_dev
+from gpu_harness import LSE_TOL, Pair, assert_close, assert_lse, bf16_dev_to_f64, to_dev
 
 pytestmark = pytest.mark.gpu
 
 W = synth.WORKLOADS
-LSE_TOL = 1e-2
 
 
 @pytest.fixture(scope="module", autouse=True)

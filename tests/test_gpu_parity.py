@@ -8,7 +8,7 @@ import torch
 from oracle import skv_oracle as O
 from streaming_kv_cache_gb300 import skv, synth
 
-from gpu_harness import Pair, assert_close, assert_lse, bf16_dev_to_f64, from_dev, to_dev
+from gpu_harness import LSE_TOL, Pair, assert_close, assert_lse, bf16_dev_to_f64, from_dev, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -21,12 +21,6 @@ def _built():
         pytest.skip("no CUDA device")
     from streaming_kv_cache_gb300 import build
     build.build()
-
-
-# LSE bound: the tensor cores take the rotated Q and K rounded to fp16
-# (relative error 2^-11 each), so a score moves by about 2^-10 |q||k| sm_scale;
-# over N(0,1) inputs that stays well under 1e-2 in the log-sum-exp.
-LSE_TOL = 1e-2
 
 
 def _prefill_check(pair, step_tag, rows=None, watch=None, lse_tol=LSE_TOL, rel=0.0, max_abs=1e-2):
@@ -110,7 +104,7 @@ def test_prefill_peaky_queries():
     pair = Pair(w, "peak")
     pair.fill()
     pair.insert()
-    _prefill_check(pair, "x", rel=2.0 ** -8)
+    _prefill_check(pair, "x", rel=2.0 ** -8, lse_tol=4 * LSE_TOL)
 
 
 def test_prefill_dominant_late_keys():
@@ -127,7 +121,7 @@ def test_prefill_dominant_late_keys():
     for view, tok in ((1, 30), (2, 5), (3, 170)):
         kf[:, view, tok] *= 30.0
     pair.insert(synth.f32_to_bf16_bits(kf), v)
-    _prefill_check(pair, "x", max_abs=5e-2, lse_tol=0.1)
+    _prefill_check(pair, "x", max_abs=5e-2, lse_tol=30 * LSE_TOL)
 
 
 @pytest.mark.parametrize("B", synth.VERIFY_BATCHES)
