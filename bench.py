@@ -365,6 +365,8 @@ def run_only(args):
         w = w.with_(tail_cap=max(w.tail_cap, args.tail_n))
     if args.only == "verify" and args.blk:
         w = w.with_(blk=args.blk)
+    if args.only == "verify" and args.tail_cap:
+        w = w.with_(tail_cap=args.tail_cap)
     mrope = None
     if args.mrope:
         # multi-section rotary: frames in rows of --mrope tokens, 5/16 of the
@@ -466,6 +468,8 @@ def main():
                     help="tail tokens of the --only tail case (after an empty tail)")
     ap.add_argument("--mrope", type=int, default=0,
                     help="multi-section rotary on the --only case, frames in rows of this many tokens")
+    ap.add_argument("--tail-cap", type=int, default=0,
+                    help="tail capacity of the --only verify case (default: the workload's 128)")
     ap.add_argument("--blk", type=int, default=None,
                     help="verify block size of the --only verify case (default: the workload's 9)")
     args = ap.parse_args()

@@ -102,6 +102,8 @@ enum {
   V_COUNT = V_DRAIN + 1
 };
 static_assert(VLayout<128>::NBAR >= V_COUNT, "barrier slots");
+// the rotation tables are read as float4
+static_assert(VLayout<128>::R64_OFF % 16 == 0 && VLayout<64>::R64_OFF % 16 == 0, "R64 alignment");
 // the merge keeps (m, l) of MAX_ROWS block rows x MAX_SPLITS pieces in the K and V stages
 static_assert(KST * VLayout<64>::KT + VST * VLayout<64>::VT >= 2 * MAX_ROWS * MAX_SPLITS * 4, "merge scratch");
 static_assert(MAX_ROWS <= QROWS, "block rows fit the query buffer");

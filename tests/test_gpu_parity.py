@@ -177,6 +177,32 @@ def test_verify_full_block_rows_uneven_tails():
     assert pair.cache.device_status() == 0
 
 
+@pytest.mark.parametrize("B", [8, 64])
+def test_verify_large_tail_capacity_uneven_tails(B):
+    """A tail capacity of 1024 rows with tails of 0 to 700 tokens in use: the
+    shares are planned for the capacity and each piece skips the key tiles
+    past its tail in use; every block row against the oracle on a spread of
+    caches."""
+    w = W["alpamayo_verify"].with_(C=B, tail_cap=1024)
+    tails = [(37 * c * c + 11 * c) % 701 for c in range(B)]
+    watch = list(range(B)) if B <= 8 else [0, 1, 2, 17, 40, 63]
+    pair = Pair(w, "vcap%d" % B, watch=watch)
+    pair.fill()
+    pair.insert()
+    tk, tv = synth.tail_kv(w, max(tails), pair.tag)
+    skv.kv_write_rows(pair.cache, pair.cache.n_visual, to_dev(tk), to_dev(tv))
+    for c in watch:
+        pair.win[c].set_tail(tk[c][:tails[c]], tv[c][:tails[c]])
+    q, k, v = synth.verify_block(w, pair.tag)
+    tail = torch.tensor(tails, dtype=torch.int32, device="cuda")
+    out, _, _ = skv.stream_attn_verify(pair.cache, tail, to_dev(q), to_dev(k), to_dev(v), w.sm_scale)
+    got = bf16_dev_to_f64(out)
+    for c in watch:
+        want, _ = O.stream_verify(pair.win[c], q[c], k[c], v[c], w.theta, w.sm_scale)
+        assert_close(got[c], want, "verify tail_cap 1024 B=%d cache %d (tail %d)" % (B, c, tails[c]))
+    assert pair.cache.device_status() == 0
+
+
 @pytest.mark.parametrize("B", [1, 8, 64])
 def test_verify_17_query_block(B):
     """A 17-query block (the last accepted token + 16 drafts): 68 block rows
