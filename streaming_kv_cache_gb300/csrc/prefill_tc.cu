@@ -67,6 +67,7 @@ constexpr int WARP_KTMA = 8, WARP_MMA = 9, WARP_VFWD = 10, WARP_VTMA = 11, WARP_
 constexpr int REG_SOFTMAX = 176, REG_CTRL = 56, REG_ROPE = 104;
 static_assert(256 * REG_SOFTMAX + 128 * REG_CTRL + 128 * REG_ROPE == 65536, "register split");
 constexpr int MAX_TILES = 1024;
+constexpr int BAR_TILES = 4;    // named barrier: the set-up warp -> the two producers
 constexpr int MAX_VIEWS = 64;
 constexpr float LAG_LIMIT = 1048576.0f;   // 2^20: a tile's probability sum that triggers a rescale
 constexpr uint64_t DRAIN_NS = 500000000ull;  // bounded wait for own in-flight copies/MMAs
@@ -234,9 +235,73 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
   const int zc = c * g.Hkv + h;                    // (cache, kv head) plane of the tensor maps
   const uint64_t wait_ns = p.wait_ns;
 
+  // The query tiles depend on nothing the set-up computes: their copy starts
+  // at entry (its barrier is initialised here, the others below).  Both
+  // tiles: rows (token, head) of kv head h, 64 columns per box.
+  if (warp == WARP_KTMA && lane == 0) {
+    tc::mbar_init(bar(B_QLOAD), 1);
+    tc::fence_barrier_init();
+    tc::fence_proxy_async_smem();
+    tc::prefetch_tmap(&tmap_q);
+    const int z0 = c * p.NQ + qoff + t0;
+    tc::mbar_arrive_expect_tx(bar(B_QLOAD), 2 * L::QT);
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+#pragma unroll
+      for (int hf = 0; hf < D / 64; ++hf)
+        tc::tma_load_3d(sbase + L::Q_OFF + i * L::QT + hf * L::HALF_Q, &tmap_q, bar(B_QLOAD), hf * 64, h * p.G,
+                        z0 + i * p.TQ);
+  }
+
+  // The copies of key tile j into stage j % NST: this CTA's 64 K rows (K
+  // producer) or its D/2 V^T rows of the 128 keys (V producer).  A 64-row
+  // block of a view's new frame comes from the step's input [C][V][T][Hkv][d]
+  // when the insert is fused: K rows as they are, V token-major (an MN-major
+  // operand for the PV product); every other block from the ring.
+  auto issue_tile = [&](bool is_k, int j) {
+    const int s = j % NST, r0 = s_tiles[j];
+    const uint32_t src = FUSED ? s_src[j] : 0u;
+    auto new_block = [&](int r, int& t_in, int& cv) {
+      const int u = r - g.P, v = u / FT;
+      t_in = u % FT % g.T;
+      cv = c * g.V + v;
+    };
+    if (is_k) {
+      tc::mbar_arrive_expect_tx(bar(B_KFULL + s), L::KST);
+      if (FUSED && (src >> rank) & 1u) {
+        int t_in, cv;
+        new_block(r0 + HN * (int)rank, t_in, cv);
+#pragma unroll
+        for (int hf = 0; hf < D / 64; ++hf)
+          tc::tma_load_4d(sbase + L::K_OFF + s * L::KST + hf * L::HALF_K, &tmap_kn, bar(B_KFULL + s), hf * 64, h,
+                          t_in, cv);
+      } else {
+#pragma unroll
+        for (int hf = 0; hf < D / 64; ++hf)
+          tc::tma_load_3d(sbase + L::K_OFF + s * L::KST + hf * L::HALF_K, &tmap_k, bar(B_KFULL + s), hf * 64,
+                          r0 + HN * (int)rank, zc);
+      }
+    } else {
+      tc::mbar_arrive_expect_tx(bar(B_VFULL + s), L::VST);
+#pragma unroll
+      for (int kh = 0; kh < 2; ++kh) {
+        if (FUSED && (src >> kh) & 1u) {
+          int t_in, cv;
+          new_block(r0 + kh * 64, t_in, cv);
+          tc::tma_load_4d(sbase + L::V_OFF + s * L::VST + kh * L::HALF_V, &tmap_vn, bar(B_VFULL + s),
+                          (D / 2) * (int)rank, h, t_in, cv);
+        } else {
+          tc::tma_load_3d(sbase + L::V_OFF + s * L::VST + kh * L::HALF_V, &tmap_v, bar(B_VFULL + s), r0 + kh * 64,
+                          (D / 2) * (int)rank, zc);
+        }
+      }
+    }
+  };
+
   if (warp == 0) {
     if (lane == 0) {
       for (int i = 0; i < B_COUNT; ++i) {
+        if (i == B_QLOAD) continue;
         // warpgroup-wide events arrive once per warp (after __syncwarp)
         int count = 1;
         if (i == B_PFULL || i == B_PFULL + 1) count = 8;      // 2 CTAs x 4 warps
@@ -305,6 +370,18 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
       *s_wrap = wrap;
       tc::fence_barrier_init();
     }
+    // the tile list and the local barriers are ready: the producers may start
+    tc::bar_arrive_n(BAR_TILES, 96);
+  }
+  if (warp == WARP_KTMA || warp == WARP_VTMA) {
+    // the first NST tiles need no free stage: their copies start before the
+    // TMEM allocation and the cluster barrier
+    tc::bar_sync_n(BAR_TILES, 96);
+    if (lane == 0) {
+      const int n0 = *s_ntiles;
+      tc::prefetch_tmap(warp == WARP_KTMA ? &tmap_k : &tmap_v);
+      for (int j = 0; j < n0 && j < NST; ++j) issue_tile(warp == WARP_KTMA, j);
+    }
   }
   if (warp == WARP_KTMA) {
     tc::tmem_alloc_pair(tc::smem_u32(s_tmem), 512);
@@ -337,69 +414,20 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
     if (warp == WARP_KTMA || warp == WARP_VTMA) {
       // -------------------------------------- producers of this CTA's halves
       const bool is_k = warp == WARP_KTMA;
-      if (lane == 0 && nt > 0) {
-        tc::prefetch_tmap(is_k ? &tmap_k : &tmap_v);
-        if (is_k) {
-          // both query tiles: rows (token, head) of kv head h, 64 columns per box
-          const int z0 = c * p.NQ + qoff + t0;
-          tc::mbar_arrive_expect_tx(bar(B_QLOAD), 2 * L::QT);
-#pragma unroll
-          for (int i = 0; i < 2; ++i)
-#pragma unroll
-            for (int hf = 0; hf < D / 64; ++hf)
-              tc::tma_load_3d(sbase + L::Q_OFF + i * L::QT + hf * L::HALF_Q, &tmap_q, bar(B_QLOAD), hf * 64,
-                              h * p.G, z0 + i * p.TQ);
-        }
-        int issued = 0;
-        for (int j = 0; j < nt; ++j) {
-          const int s = j % NST, u = j / NST, r0 = s_tiles[j];
-          if (j >= NST &&
-              !tc::mbar_wait_cluster<SW>(bar((is_k ? B_KEMPTY : B_VEMPTY) + s), (u - 1) & 1, wait_ns, s_abort))
+      if (lane == 0) {
+        // tiles [0, NST) were issued before the cluster barrier
+        int issued = min(nt, NST);
+        for (int j = NST; j < nt; ++j) {
+          const int s = j % NST, u = j / NST;
+          if (!tc::mbar_wait_cluster<SW>(bar((is_k ? B_KEMPTY : B_VEMPTY) + s), (u - 1) & 1, wait_ns, s_abort))
             break;
-          // a 64-row block of a view's new frame comes from the step's input
-          // [C][V][T][Hkv][d]: K rows as they are, V token-major (an MN-major
-          // operand for the PV product); every other block from the ring
-          const uint32_t src = FUSED ? s_src[j] : 0u;
-          auto new_block = [&](int r, int& t_in, int& cv) {
-            const int u = r - g.P, v = u / FT;
-            t_in = u % FT % g.T;
-            cv = c * g.V + v;
-          };
-          if (is_k) {
-            tc::mbar_arrive_expect_tx(bar(B_KFULL + s), L::KST);
-            if (FUSED && (src >> rank) & 1u) {
-              int t_in, cv;
-              new_block(r0 + HN * (int)rank, t_in, cv);
-#pragma unroll
-              for (int hf = 0; hf < D / 64; ++hf)
-                tc::tma_load_4d(sbase + L::K_OFF + s * L::KST + hf * L::HALF_K, &tmap_kn, bar(B_KFULL + s), hf * 64,
-                                h, t_in, cv);
-            } else {
-#pragma unroll
-              for (int hf = 0; hf < D / 64; ++hf)
-                tc::tma_load_3d(sbase + L::K_OFF + s * L::KST + hf * L::HALF_K, &tmap_k, bar(B_KFULL + s), hf * 64,
-                                r0 + HN * (int)rank, zc);
-            }
-          } else {
-            tc::mbar_arrive_expect_tx(bar(B_VFULL + s), L::VST);
-#pragma unroll
-            for (int kh = 0; kh < 2; ++kh) {
-              if (FUSED && (src >> kh) & 1u) {
-                int t_in, cv;
-                new_block(r0 + kh * 64, t_in, cv);
-                tc::tma_load_4d(sbase + L::V_OFF + s * L::VST + kh * L::HALF_V, &tmap_vn, bar(B_VFULL + s),
-                                (D / 2) * (int)rank, h, t_in, cv);
-              } else {
-                tc::tma_load_3d(sbase + L::V_OFF + s * L::VST + kh * L::HALF_V, &tmap_v, bar(B_VFULL + s),
-                                r0 + kh * 64, (D / 2) * (int)rank, zc);
-              }
-            }
-          }
+          issue_tile(is_k, j);
           issued = j + 1;
         }
         if (*s_abort) set_status(p.status, SKV_DEV_TIMEOUT);
         // the copies this thread started land before the CTA exits, whether or
-        // not their consumers (which may have given up) waited for them
+        // not their consumers (which may have given up) waited for them (the
+        // query tiles are copied for every item, even one without key tiles)
         if (is_k) {
           volatile int never = 0;
           tc::mbar_wait<SW>(bar(B_QLOAD), 0, DRAIN_NS, &never);
@@ -652,34 +680,39 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
       // t0 + qi*TQ + r/G, head r%G); rotate in place, at each token's
       // logical position, into fp16.  Thread tid takes chunk ch (8
       // frequencies) of NCH consecutive rows, four rows at a time.
+      constexpr int HALF = D / 2, NCH = HALF / 8;
+      const int ch = tid % NCH, rr0 = (tid / NCH) * NCH;
+      const int ea = ch * 8, eb = HALF + ch * 8;
+      const uint32_t off_a = (ea / 64) * L::HALF_Q, off_b = (eb / 64) * L::HALF_Q;
+      const int ca = (ea % 64) / 8, cb = (eb % 64) / 8;
+      const float4* rope4 = reinterpret_cast<const float4*>(p.rope);
+      // the table entries of every row first: they depend only on the rows'
+      // positions, so their loads overlap the queries' copy
+      float4 cs[NCH][4];
+#pragma unroll
+      for (int q = 0; q < NCH; ++q) {
+        const int rr = rr0 + q, qi = rr >> 7, r = rr & 127;
+        const int qtok = min(t0 + qi * p.TQ + r / p.G, n_seg - 1);
+#pragma unroll
+        for (int w4 = 0; w4 < 4; ++w4) cs[q][w4] = __ldg(rope4 + ((size_t)(pos0 + qtok) * HALF + ea) / 2 + w4);
+      }
       ok = __all_sync(0xffffffffu, tc::mbar_wait<SW>(bar(B_QLOAD), 0, wait_ns, s_abort));
       if (ok) {
-        constexpr int HALF = D / 2, NCH = HALF / 8;
-        const int ch = tid % NCH, rr0 = (tid / NCH) * NCH;
-        const int ea = ch * 8, eb = HALF + ch * 8;
-        const uint32_t off_a = (ea / 64) * L::HALF_Q, off_b = (eb / 64) * L::HALF_Q;
-        const int ca = (ea % 64) / 8, cb = (eb % 64) / 8;
-        const float4* rope4 = reinterpret_cast<const float4*>(p.rope);
-
 #pragma unroll
         for (int b4 = 0; b4 < NCH; b4 += 4) {
           uint4 xa[4], xb[4];
-          float4 cs[4][4];
           uint8_t* rp[4];
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             const int rr = rr0 + b4 + q, qi = rr >> 7, r = rr & 127;
-            const int qtok = min(t0 + qi * p.TQ + r / p.G, n_seg - 1);
             rp[q] = smem + L::Q_OFF + qi * L::QT;
             xa[q] = *reinterpret_cast<const uint4*>(rp[q] + off_a + tc::sw128_off(r, ca));
             xb[q] = *reinterpret_cast<const uint4*>(rp[q] + off_b + tc::sw128_off(r, cb));
-#pragma unroll
-            for (int w4 = 0; w4 < 4; ++w4) cs[q][w4] = __ldg(rope4 + ((size_t)(pos0 + qtok) * HALF + ea) / 2 + w4);
           }
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             const int r = (rr0 + b4 + q) & 127;
-            rotate_pairs4(xa[q], xb[q], cs[q]);
+            rotate_pairs4(xa[q], xb[q], cs[b4 + q]);
             *reinterpret_cast<uint4*>(rp[q] + off_a + tc::sw128_off(r, ca)) = xa[q];
             *reinterpret_cast<uint4*>(rp[q] + off_b + tc::sw128_off(r, cb)) = xb[q];
           }

@@ -295,6 +295,14 @@ __device__ __forceinline__ void tma_store_commit_wait_read() {
   asm volatile("cp.async.bulk.commit_group;\ncp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
+// Named barrier id over n threads: wait for all of them / arrive without waiting.
+__device__ __forceinline__ void bar_sync_n(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+__device__ __forceinline__ void bar_arrive_n(int id, int n) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
 // Named barrier over n threads that also ANDs a predicate across them.
 __device__ __forceinline__ bool bar_and(int id, int n, bool v) {
   uint32_t r;
