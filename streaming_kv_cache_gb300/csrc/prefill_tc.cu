@@ -687,14 +687,22 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
       const int ca = (ea % 64) / 8, cb = (eb % 64) / 8;
       const float4* rope4 = reinterpret_cast<const float4*>(p.rope);
       // the table entries of every row first: they depend only on the rows'
-      // positions, so their loads overlap the queries' copy
+      // positions, so their loads overlap the queries' copy.  Rows of one
+      // token (its G heads) share them: one load per token.
       float4 cs[NCH][4];
+      int prev_tok = -1;
 #pragma unroll
       for (int q = 0; q < NCH; ++q) {
         const int rr = rr0 + q, qi = rr >> 7, r = rr & 127;
         const int qtok = min(t0 + qi * p.TQ + r / p.G, n_seg - 1);
+        if (q > 0 && qtok == prev_tok) {
 #pragma unroll
-        for (int w4 = 0; w4 < 4; ++w4) cs[q][w4] = __ldg(rope4 + ((size_t)(pos0 + qtok) * HALF + ea) / 2 + w4);
+          for (int w4 = 0; w4 < 4; ++w4) cs[q][w4] = cs[q - 1][w4];
+        } else {
+#pragma unroll
+          for (int w4 = 0; w4 < 4; ++w4) cs[q][w4] = __ldg(rope4 + ((size_t)(pos0 + qtok) * HALF + ea) / 2 + w4);
+        }
+        prev_tok = qtok;
       }
       ok = __all_sync(0xffffffffu, tc::mbar_wait<SW>(bar(B_QLOAD), 0, wait_ns, s_abort));
       if (ok) {

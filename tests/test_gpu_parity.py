@@ -124,6 +124,27 @@ def test_prefill_dominant_late_keys():
     _prefill_check(pair, "x", max_abs=5e-2, lse_tol=30 * LSE_TOL)
 
 
+@pytest.mark.parametrize("half", [0, 1])
+def test_prefill_dominant_key_in_either_half_of_a_tile(half):
+    """One key of view 1's newest frame, 30x larger than the rest, placed at
+    an offset of its 128-key tile in the first (0-63) or the second (64-127)
+    half: the running max of every row that sees it jumps on that tile, and
+    the rescale must cover the tile's keys on both sides of the large one."""
+    w = W["alpamayo_step"].with_(C=1)
+    pair = Pair(w, "domh%d" % half)
+    pair.fill()
+    view = 1
+    slot = int(pair.cache.head.cpu().numpy()[0][view])      # the slot the next insert writes
+    row0 = w.P + (view * w.F + slot) * w.T
+    # the first token of the frame whose row offset in its tile lies in the half
+    tok = next(t for t in range(w.T) if ((row0 + t) % 128) // 64 == half and (row0 + t) % 64 >= 8)
+    k, v = synth.frame_kv(w, pair.n_inserts, pair.tag)
+    kf = O.bf16_to_f64(k).astype(np.float32)
+    kf[:, view, tok] *= 30.0
+    pair.insert(synth.f32_to_bf16_bits(kf), v)
+    _prefill_check(pair, "x", max_abs=5e-2, lse_tol=30 * LSE_TOL)
+
+
 @pytest.mark.parametrize("B", synth.VERIFY_BATCHES)
 def test_verify_alpamayo_batches(B):
     w = W["alpamayo_verify"].with_(C=B)
