@@ -354,10 +354,10 @@ size_t skv_verify_workspace_bytes(const skv_cache* cache, int32_t n_q_head, int3
  *     Calls that may run at the same time (other streams) need workspaces
  *     of their own: the arrival counters in it are per call.
  * Needs 1 <= blk <= tail_cap, V <= 64 and Hq/Hkv <= 64 (else
- * SKV_ERR_UNSUPPORTED); a block of more than 64 rows per kv head
- * (blk * Hq/Hkv) is taken 64 rows at a time, which needs Hq/Hkv to divide
- * 64.  tail_len + blk > tail_cap sets SKV_DEV_TAIL_OVERFLOW and skips that
- * cache.
+ * SKV_ERR_UNSUPPORTED).  A block of up to 128 rows per kv head
+ * (blk * Hq/Hkv) streams the keys once; a larger one is taken 128 rows at a
+ * time, which needs Hq/Hkv to divide 128.  tail_len + blk > tail_cap sets
+ * SKV_DEV_TAIL_OVERFLOW and skips that cache.
  */
 int stream_attn_verify(const skv_cache* cache, int32_t n_q_head, int32_t blk,
                        const int32_t* tail_len, const void* q_blk, const void* k_blk,

@@ -317,9 +317,9 @@ int stream_attn_verify(const skv_cache* cache, int32_t n_q_head, int32_t blk,
   if (n_q_head < 1 || n_q_head % cache->n_kv_head) return SKV_ERR_INVALID;
   if (blk < 1 || blk > cache->tail_cap) return SKV_ERR_INVALID;
   {
-    // block rows are taken 64 at a time per kv head, whole tokens each
+    // block rows are taken 64 (more than 64: 128) at a time per kv head, whole tokens each
     const int G = n_q_head / cache->n_kv_head;
-    if (G > 64 || ((long long)blk * G > 64 && 64 % G)) return SKV_ERR_UNSUPPORTED;
+    if (G > 64 || ((long long)blk * G > 128 && 128 % G)) return SKV_ERR_UNSUPPORTED;
   }
   if (!(sm_scale > 0.f) || sm_scale != sm_scale) return SKV_ERR_INVALID;
   if (cache->n_cache == 0) return SKV_OK;

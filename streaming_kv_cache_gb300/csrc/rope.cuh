@@ -117,17 +117,18 @@ __device__ __forceinline__ void rotate_key_rows(uint8_t* kt, uint32_t off_a, uin
                                                 const int* heads, const float4* rope4, int ea, int half) {
   if (run >= NPT && r0 + NPT <= row_lim) {
     // two rows in flight at a time (registers)
+    constexpr int IF = NPT >= 2 ? 2 : 1;
     Ang8 ang = ang8_from(first);
 #pragma unroll
-    for (int k0 = 0; k0 < NPT; k0 += 2) {
-      uint4 xa[2], xb[2];
+    for (int k0 = 0; k0 < NPT; k0 += IF) {
+      uint4 xa[IF], xb[IF];
 #pragma unroll
-      for (int k = 0; k < 2; ++k) {
+      for (int k = 0; k < IF; ++k) {
         xa[k] = *reinterpret_cast<const uint4*>(kt + off_a + tc::sw128_off(row_base + k0 + k, ca));
         xb[k] = *reinterpret_cast<const uint4*>(kt + off_b + tc::sw128_off(row_base + k0 + k, cb));
       }
 #pragma unroll
-      for (int k = 0; k < 2; ++k) {
+      for (int k = 0; k < IF; ++k) {
         if (k0 + k > 0) ang8_step(ang, step);
         rotate8(xa[k], xb[k], ang);
         *reinterpret_cast<uint4*>(kt + off_a + tc::sw128_off(row_base + k0 + k, ca)) = xa[k];

@@ -18,10 +18,10 @@
 // merges them after its CTA's key loop.
 //
 // Per piece the query buffer holds the unit's blk x G block rows in its 64
-// rows; the M=128 MMA reads its rows 64-127 from whatever shared memory
-// follows, and their S and O rows (TMEM lanes 64-127) are never read.  Most
-// MMA rows are idle: the kernel is bound by streaming K and V^T from HBM, not
-// by the tensor cores.  The query block lands by TMA and is rotated in place;
+// rows (the WIDE form below: 128); the M=128 MMA reads rows past them from
+// whatever shared memory follows, and their S and O rows (TMEM lanes) are
+// never read.  Most MMA rows are idle: the kernel is bound by streaming K and
+// V^T from HBM, not by the tensor cores.  The query block lands by TMA and is rotated in place;
 // 64-key tiles flow through a 3-stage TMA ring for K (a stage is held while
 // its tile is rotated) and a 2-stage one for V^T; RoPE is applied to each K
 // tile in shared memory (fp16 out), S double-buffers in TMEM so QK of tile
@@ -33,6 +33,10 @@
 //   warp  3    V^T producer
 //   warp  4    MMA issuer
 //   warps 5-8  RoPE (query block of every piece, then its K tiles)
+// The WIDE form (blocks of more than 64 rows per kv head, one CTA per SM):
+//   warps 0-3  softmax + epilogue (TMEM lanes 0-127)
+//   warps 4-6  K producer, V^T producer, MMA issuer; warp 7 idle
+//   warps 8-15 RoPE
 #include <cudaTypedefs.h>
 #include <math.h>
 
@@ -49,13 +53,6 @@ namespace {
 
 constexpr int BM = 128;     // query-tile rows (block rows; the rest unused)
 constexpr int BN = 64;      // keys per tile
-constexpr int KST = 3;      // K stages (a K tile is held through its rotation)
-constexpr int VST = 2;      // V^T stages
-constexpr int QROWS = 64;   // query rows kept in shared memory (block rows)
-constexpr int NTHREADS = 288;
-constexpr int WARP_KTMA = 2, WARP_VTMA = 3, WARP_MMA = 4, WARP_ROPE = 5;
-constexpr int SOFTMAX_THREADS = 64;
-constexpr int MAX_ROWS = 64;     // block rows per kv head (TMEM lanes of the softmax warps)
 constexpr int MAX_VIEWS = 64;
 constexpr int MAX_PIECES = 16;   // pieces of one CTA's share
 constexpr int MAX_SPLITS = 64;   // pieces of one unit
@@ -63,8 +60,56 @@ constexpr int MIN_SHARE = 4;     // key tiles per CTA at least
 constexpr float RESCALE_THRESHOLD = 8.0f;
 constexpr uint64_t DRAIN_NS = 500000000ull;
 
-template <int D>
+// Two forms of the kernel.  NARROW: units of up to 64 block rows, two
+// softmax warps (TMEM lanes 0-63), four RoPE warps, two CTAs per SM.  WIDE,
+// for blocks of more than 64 rows per kv head (17 tokens x 4 heads, say):
+// units of up to 128 rows, four softmax warps (lanes 0-127), eight RoPE
+// warps and one CTA per SM, so that a plane's keys stream once for all of
+// its block rows.
+template <bool WIDE>
+struct VCfg {
+  static constexpr int ROWS = WIDE ? 128 : 64;     // block rows of a unit at most
+  static constexpr int SM_WARPS = ROWS / 32;       // softmax warps: TMEM lanes [0, ROWS)
+  static constexpr int WARP_KTMA = SM_WARPS, WARP_VTMA = SM_WARPS + 1, WARP_MMA = SM_WARPS + 2;
+  static constexpr int WARP_ROPE = WIDE ? 8 : 5;   // (WIDE: warp 7 has no role)
+  static constexpr int ROPE_WARPS = WIDE ? 8 : 4;
+  static constexpr int NT = (WARP_ROPE + ROPE_WARPS) * 32;
+  static constexpr int CTAS_PER_SM = WIDE ? 1 : 2;
+  // K stages (a K tile is held through its rotation) and V^T stages: one
+  // CTA per SM keeps as many bytes in flight as two of the narrow form
+  static constexpr int KST = WIDE ? 6 : 3;
+  static constexpr int VST = WIDE ? 4 : 2;
+  // S buffers in TMEM (BN columns each; O follows them): the MMA issuer runs
+  // QK up to NS - 1 tiles ahead of PV
+  static constexpr int NS = WIDE ? 4 : 2;
+  static constexpr int TMEM_COLS = WIDE ? 512 : 256;
+};
+
+// mbarrier slots for KST K stages and VST V^T stages
+template <int KST, int VST, int NS>
+struct VBars {
+  enum : int {
+    QLOAD = 0,                  // query block landed (TMA)
+    QFULL = 1,                  // RoPE warps: query block rotated
+    QEMPTY = 2,                 // MMA commit: the piece's QK MMAs are done with it
+    KFULL = 3,                  // K tile landed
+    KROT = KFULL + KST,         // RoPE warps: K tile rotated
+    KEMPTY = KROT + KST,        // MMA commit: K stage free
+    VFULL = KEMPTY + KST,       // V^T tile landed
+    VEMPTY = VFULL + VST,       // MMA commit: V^T stage free
+    SFULL = VEMPTY + VST,       // MMA commit: S buffer ready (NS)
+    PFULL = SFULL + NS,         // softmax warps: P in the S buffer (NS)
+    PVDONE = PFULL + NS,        // MMA commit: the PV of a tile landed in O (NS: one per S buffer)
+    ODONE = PVDONE + NS,        // MMA commit: the piece's last PV landed
+    OFREE = ODONE + 1,          // softmax warps: O read out
+    DRAIN = OFREE + 1,          // MMA commit: everything issued is complete
+    COUNT = DRAIN + 1
+  };
+};
+
+template <int D, bool WIDE>
 struct VLayout {
+  static constexpr int QROWS = VCfg<WIDE>::ROWS;   // query rows kept in shared memory (block rows)
   static constexpr int QT = QROWS * D * 2;
   static constexpr int KT = BN * D * 2;   // 64 rows x D
   static constexpr int VT = D * BN * 2;   // D rows x 64 keys (one 128-byte-swizzled box)
@@ -72,41 +117,26 @@ struct VLayout {
   static constexpr int HALF_K = BN * 128;
   static constexpr int Q_OFF = 0;
   static constexpr int K_OFF = Q_OFF + QT;
+  static constexpr int KST = VCfg<WIDE>::KST, VST = VCfg<WIDE>::VST;
   static constexpr int V_OFF = K_OFF + KST * KT;
-  static constexpr int BAR_OFF = V_OFF + VST * VT;
-  static constexpr int NBAR = 24;
+  // the merge keeps (m, l) of ROWS block rows x MAX_SPLITS pieces in the K
+  // and V stages (extended where they are smaller)
+  static constexpr int SCRATCH = 2 * QROWS * MAX_SPLITS * 4;
+  static constexpr int BAR_OFF = (V_OFF + VST * VT > K_OFF + SCRATCH ? V_OFF + VST * VT : K_OFF + SCRATCH);
+  static constexpr int NBAR = (VBars<KST, VST, VCfg<WIDE>::NS>::COUNT + 1) / 2 * 2;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
   static constexpr int PIECE_OFF = MISC_OFF + 64;                 // MAX_PIECES x 8 ints
   static constexpr int MERGE_OFF = PIECE_OFF + MAX_PIECES * 32;   // units to merge
-  static constexpr int HEAD_OFF = MERGE_OFF + MAX_PIECES * 4;     // 4 RoPE warps x MAX_VIEWS heads
-  static constexpr int R64_OFF = HEAD_OFF + 4 * MAX_VIEWS * 4;     // 4 RoPE warps x R(BN) of every chunk
-  static constexpr int BYTES = R64_OFF + 4 * (D / 16) * 64;
+  static constexpr int HEAD_OFF = MERGE_OFF + MAX_PIECES * 4;     // per RoPE warp: MAX_VIEWS heads
+  static constexpr int R64_OFF = HEAD_OFF + VCfg<WIDE>::ROPE_WARPS * MAX_VIEWS * 4;  // per RoPE warp: R(BN) of every chunk
+  static constexpr int BYTES = R64_OFF + VCfg<WIDE>::ROPE_WARPS * (D / 16) * 64;
   static constexpr int ALLOC = BYTES + 1024;
 };
 
-enum {
-  V_QLOAD = 0,                  // query block landed (TMA)
-  V_QFULL = 1,                  // 4 RoPE warps: query block rotated
-  V_QEMPTY = 2,                 // MMA commit: the piece's QK MMAs are done with it
-  V_KFULL = 3,                  // K tile landed
-  V_KROT = V_KFULL + KST,       // 4 RoPE warps: K tile rotated
-  V_KEMPTY = V_KROT + KST,      // MMA commit: K stage free
-  V_VFULL = V_KEMPTY + KST,     // V^T tile landed
-  V_VEMPTY = V_VFULL + VST,     // MMA commit: V^T stage free
-  V_SFULL = V_VEMPTY + VST,     // MMA commit: S buffer ready (2)
-  V_PFULL = V_SFULL + 2,        // 2 softmax warps: P in the S buffer (2)
-  V_PVDONE = V_PFULL + 2,       // MMA commit: a PV landed in O
-  V_ODONE = V_PVDONE + 1,       // MMA commit: the piece's last PV landed
-  V_OFREE = V_ODONE + 1,        // 2 softmax warps: O read out
-  V_DRAIN = V_OFREE + 1,        // MMA commit: everything issued is complete
-  V_COUNT = V_DRAIN + 1
-};
-static_assert(VLayout<128>::NBAR >= V_COUNT, "barrier slots");
 // the rotation tables are read as float4
-static_assert(VLayout<128>::R64_OFF % 16 == 0 && VLayout<64>::R64_OFF % 16 == 0, "R64 alignment");
-// the merge keeps (m, l) of MAX_ROWS block rows x MAX_SPLITS pieces in the K and V stages
-static_assert(KST * VLayout<64>::KT + VST * VLayout<64>::VT >= 2 * MAX_ROWS * MAX_SPLITS * 4, "merge scratch");
-static_assert(MAX_ROWS <= QROWS, "block rows fit the query buffer");
+static_assert(VLayout<128, false>::R64_OFF % 16 == 0 && VLayout<64, false>::R64_OFF % 16 == 0 &&
+                  VLayout<128, true>::R64_OFF % 16 == 0 && VLayout<64, true>::R64_OFF % 16 == 0,
+              "R64 alignment");
 
 // One piece of a CTA's share: tiles [ta, ta + nt) of unit u, piece k of the
 // unit's n, whose cache has tl tail tokens; g0 = the CTA's tiles before it.
@@ -115,7 +145,7 @@ enum { PC_U = 0, PC_TA, PC_NT, PC_TL, PC_K, PC_N, PC_OK, PC_G0 };
 struct VerifyParams {
   Geom g;
   int Hq, G, blk, R;          // R = blk * G block rows per kv head
-  int RH, RU, TQH;            // row halves per kv head (64 block rows each), rows per unit at most, tokens per query box
+  int RH, RU, TQH;            // row units per kv head (ROWS block rows each), rows per unit at most, tokens per query box
   int TM, W, P_max;           // tiles per unit, tiles per CTA, pieces per unit at most
   int units;
   const int32_t* tail_len;
@@ -138,12 +168,13 @@ __host__ __device__ __forceinline__ int last_cta(long long u, int TM, int W) { r
 // (shared memory, 2 x R x n floats) for the pieces' (m, l), then the per-row
 // weights.  The partials are read from L2 with many loads in flight: this
 // runs once the CTA's keys are done, on the kernel's tail.
-template <int D>
+template <int D, bool WIDE>
 __device__ __noinline__ void merge_pieces(const VerifyParams& p, int u, int n, int tid, float* wts) {
+  constexpr int NTHREADS = VCfg<WIDE>::NT;
   const size_t base = (size_t)u * p.P_max;
   const int plane = u / p.RH, rh = u % p.RH;
   const int c = plane / p.g.Hkv, h = plane % p.g.Hkv;
-  const int row0 = rh * MAX_ROWS;                    // first block row of this unit
+  const int row0 = rh * VCfg<WIDE>::ROWS;            // first block row of this unit
   const int R = min(p.RU, p.R - row0);               // its rows
   const int RS = p.RU;                               // row stride of the workspace
   float* wm = wts;           // [n][R]: m, then the weight
@@ -229,18 +260,29 @@ __device__ __noinline__ void merge_pieces(const VerifyParams& p, int u, int n, i
 }
 
 // SW: compiled for a wait limit under the suspend hint (see tc::bounded_wait)
-template <int D, bool SW>
-__global__ void __launch_bounds__(NTHREADS, 2)
+template <int D, bool SW, bool WIDE>
+__global__ void __launch_bounds__(VCfg<WIDE>::NT, VCfg<WIDE>::CTAS_PER_SM)
 verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                  const __grid_constant__ CUtensorMap tmap_q, const VerifyParams p) {
-  using L = VLayout<D>;
+  using L = VLayout<D, WIDE>;
+  using C = VCfg<WIDE>;
+  constexpr int WARP_KTMA = C::WARP_KTMA, WARP_VTMA = C::WARP_VTMA, WARP_MMA = C::WARP_MMA;
+  constexpr int WARP_ROPE = C::WARP_ROPE;
+  constexpr int SOFTMAX_THREADS = C::ROWS;
+  constexpr int NRT = C::ROPE_WARPS * 32;   // RoPE threads
+  constexpr int KST = C::KST, VST = C::VST, NS = C::NS;
+  using VB = VBars<KST, VST, NS>;
+  constexpr int V_QLOAD = VB::QLOAD, V_QFULL = VB::QFULL, V_QEMPTY = VB::QEMPTY, V_KFULL = VB::KFULL;
+  constexpr int V_KROT = VB::KROT, V_KEMPTY = VB::KEMPTY, V_VFULL = VB::VFULL, V_VEMPTY = VB::VEMPTY;
+  constexpr int V_SFULL = VB::SFULL, V_PFULL = VB::PFULL, V_PVDONE = VB::PVDONE, V_ODONE = VB::ODONE;
+  constexpr int V_OFREE = VB::OFREE, V_DRAIN = VB::DRAIN, V_COUNT = VB::COUNT;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = tc::smem_u32(smem);
   auto bar = [&](int i) { return sbase + L::BAR_OFF + 8u * i; };
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + L::MISC_OFF);
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + L::MISC_OFF + 4);
-  // [0] piece count, [1] units to merge, [2..3] the softmax warps' verdicts
+  // [0] piece count, [1] units to merge, [2..] the softmax warps' verdicts
   volatile int* s_info = reinterpret_cast<volatile int*>(smem + L::MISC_OFF + 8);
   int* s_piece = reinterpret_cast<int*>(smem + L::PIECE_OFF);
   int* s_merge = reinterpret_cast<int*>(smem + L::MERGE_OFF);
@@ -253,8 +295,8 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
     if (lane == 0) {
       for (int i = 0; i < V_COUNT; ++i) {
         int count = 1;
-        if (i == V_QFULL || (i >= V_KROT && i < V_KROT + KST)) count = 4;   // RoPE warps
-        if (i == V_PFULL || i == V_PFULL + 1 || i == V_OFREE) count = SOFTMAX_THREADS / 32;
+        if (i == V_QFULL || (i >= V_KROT && i < V_KROT + KST)) count = C::ROPE_WARPS;
+        if ((i >= V_PFULL && i < V_PFULL + NS) || i == V_OFREE) count = C::SM_WARPS;
         tc::mbar_init(bar(i), count);
       }
       *s_abort = 0;
@@ -303,7 +345,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
     }
   }
   if (warp == WARP_KTMA) {
-    tc::tmem_alloc(tc::smem_u32(s_tmem), 256);
+    tc::tmem_alloc(tc::smem_u32(s_tmem), C::TMEM_COLS);
     tc::tmem_relinquish();
   }
   tc::tc_fence_before();
@@ -365,7 +407,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
       auto issue_qk = [&](int gg) {
         const uint64_t dk = tc::opaque(dk0 + ((uint32_t)((gg % KST) * L::KT) >> 4));
         const uint64_t dq = tc::opaque(dq0);
-        const uint32_t d_tmem = tmem + (gg & 1) * BN;
+        const uint32_t d_tmem = tmem + (gg % NS) * BN;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t offq = ((kk >> 2) * L::HALF_Q + (kk & 3) * 32) >> 4;
@@ -379,16 +421,17 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
       auto issue_pv = [&](int gg, bool first) {
         const int vs = gg % VST, vu = gg / VST;
         if (!(ok = tc::mbar_wait_short<SW>(bar(V_VFULL + vs), vu & 1, wait_ns, s_abort))) return;
-        if (!(ok = tc::mbar_wait_short<SW>(bar(V_PFULL + (gg & 1)), (gg >> 1) & 1, wait_ns, s_abort))) return;
+        if (!(ok = tc::mbar_wait_short<SW>(bar(V_PFULL + gg % NS), (gg / NS) & 1, wait_ns, s_abort))) return;
         // the softmax warps have read the previous piece's O out
         if (first && a > 0 && !(ok = tc::mbar_wait_short<SW>(bar(V_OFREE), (a - 1) & 1, wait_ns, s_abort))) return;
         tc::tc_fence_after();
         const uint64_t dv = tc::opaque(dv0 + ((uint32_t)(vs * L::VT) >> 4));
-        const uint32_t a_tmem = tmem + (gg & 1) * BN;
+        const uint32_t a_tmem = tmem + (gg % NS) * BN;
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)
-          tc::mma_ts(tmem + 128, a_tmem + kk * 8, dv + (((kk & 3) * 32) >> 4), idesc_pv, (!first || kk > 0) ? 1u : 0u);
-        tc::mma_commit(bar(V_PVDONE));
+          tc::mma_ts(tmem + NS * BN, a_tmem + kk * 8, dv + (((kk & 3) * 32) >> 4), idesc_pv,
+                     (!first || kk > 0) ? 1u : 0u);
+        tc::mma_commit(bar(V_PVDONE + gg % NS));
         tc::mma_commit(bar(V_VEMPTY + vs));
       };
       int gt = 0;
@@ -396,17 +439,21 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         const int nt = P(pi, PC_NT);
         if (nt == 0) continue;
         if (!(ok = tc::mbar_wait_short<SW>(bar(V_QFULL), a & 1, wait_ns, s_abort))) break;
-        for (int j = 0; ok && j < nt; ++j) {
+        // step j: QK of the piece's tile j, then PV of its tile j - (NS - 1)
+        // (S buffer of tile j is free: the PV of tile j - NS went out a step
+        // earlier, and the tensor pipe runs in issue order)
+        for (int j = 0; ok && j < nt + NS - 1; ++j) {
           const int gg = gt + j;
-          if (!(ok = tc::mbar_wait_short<SW>(bar(V_KROT + gg % KST), (gg / KST) & 1, wait_ns, s_abort))) break;
-          tc::tc_fence_after();
-          issue_qk(gg);
-          tc::mma_commit(bar(V_SFULL + (gg & 1)));
-          tc::mma_commit(bar(V_KEMPTY + gg % KST));
-          if (j == nt - 1) tc::mma_commit(bar(V_QEMPTY));
-          if (j >= 1) issue_pv(gg - 1, j == 1);
+          if (j < nt) {
+            if (!(ok = tc::mbar_wait_short<SW>(bar(V_KROT + gg % KST), (gg / KST) & 1, wait_ns, s_abort))) break;
+            tc::tc_fence_after();
+            issue_qk(gg);
+            tc::mma_commit(bar(V_SFULL + gg % NS));
+            tc::mma_commit(bar(V_KEMPTY + gg % KST));
+            if (j == nt - 1) tc::mma_commit(bar(V_QEMPTY));
+          }
+          if (j >= NS - 1) issue_pv(gg - (NS - 1), j == NS - 1);
         }
-        if (ok) issue_pv(gt + nt - 1, nt == 1);
         if (ok) tc::mma_commit(bar(V_ODONE));
         gt += nt;
         ++a;
@@ -419,14 +466,14 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
     }
   } else if (warp >= WARP_ROPE) {
     // ----------------------------------------------------------------- RoPE
-    const int rt = tid - WARP_ROPE * 32;   // 0..127
+    const int rt = tid - WARP_ROPE * 32;   // 0 .. NRT-1
     const int wr = rt >> 5, ln = rt & 31;
     constexpr int HALF = D / 2;
     constexpr int NCH = HALF / 8;
-    constexpr int NPT = BN * NCH / 128;   // key rows per thread
+    constexpr int NPT = BN * NCH / NRT;   // key rows per thread
     int* s_head = reinterpret_cast<int*>(smem + L::HEAD_OFF) + wr * MAX_VIEWS;   // this warp's copy
     const int ch = ln % NCH;
-    const int row_base = wr * 16 + (ln / NCH) * NPT;
+    const int row_base = wr * (BN / C::ROPE_WARPS) + (ln / NCH) * NPT;
     const int ea = ch * 8, eb = HALF + ch * 8;
     const uint32_t off_a = (ea / 64) * L::HALF_K, off_b = (eb / 64) * L::HALF_K;
     const int ca = (ea % 64) / 8, cb = (eb % 64) / 8;
@@ -449,7 +496,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
       if (nt == 0) continue;
       const int u = P(pi, PC_U), ta = P(pi, PC_TA);
       const int plane = u / p.RH, c = plane / g.Hkv, h = plane % g.Hkv;
-      const int row0 = (u % p.RH) * MAX_ROWS, R_u = min(p.RU, p.R - row0);   // this unit's block rows
+      const int row0 = (u % p.RH) * C::ROWS, R_u = min(p.RU, p.R - row0);   // this unit's block rows
       const int q_base = g.n_visual() + P(pi, PC_TL);   // logical index of block token 0
       for (int v = ln; v < g.V; v += 32) s_head[v] = p.head[(size_t)c * g.V + v];
       __syncwarp();
@@ -467,7 +514,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
       if (!(ok = tc::mbar_wait<SW>(bar(V_QLOAD), a & 1, wait_ns, s_abort))) break;
       q_in_flight = false;
       // rotate the block rows in place at their tokens' positions (fp16 out)
-      for (int it = rt; it < R_u * NCH; it += 128) {
+      for (int it = rt; it < R_u * NCH; it += NRT) {
         const int n = it / NCH, cq = it % NCH;
         const int qa = cq * 8, qb = HALF + cq * 8;
         uint4* pa = reinterpret_cast<uint4*>(smem + L::Q_OFF + (qa / 64) * L::HALF_Q + tc::sw128_off(n, (qa % 64) / 8));
@@ -536,11 +583,11 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         tc::mbar_wait<SW>(bar(V_QLOAD), a & 1, DRAIN_NS, &never);
       }
     }
-  } else {
+  } else if (warp < C::SM_WARPS) {
     // ------------------------------------------------- softmax + epilogue
-    const int row = warp * 32 + lane;            // TMEM lane = the unit's block row (warps 0, 1)
+    const int row = warp * 32 + lane;            // TMEM lane = the unit's block row
     const uint32_t t_lane = (uint32_t)(warp * 32) << 16;
-    const uint32_t tO = tmem + t_lane + 128;
+    const uint32_t tO = tmem + t_lane + NS * BN;
     const float sl = p.scale_log2;
     int gt = 0, a = 0;
     bool alive = true;
@@ -548,7 +595,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
       if (!P(pi, PC_OK)) continue;      // a skipped cache: no piece of its units arrives
       const int nt = P(pi, PC_NT), u = P(pi, PC_U), n_unit = P(pi, PC_N);
       const int plane = u / p.RH, c = plane / g.Hkv, h = plane % g.Hkv;
-      const int brow = (u % p.RH) * MAX_ROWS + row;   // block row of this lane
+      const int brow = (u % p.RH) * C::ROWS + row;   // block row of this lane
       const bool valid = brow < p.R;
       const int jt = valid ? brow / p.G : 0;
       const int gq = valid ? brow % p.G : 0;
@@ -559,9 +606,9 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
       bool ok = true;
 #pragma unroll 1
       for (int j = 0; j < nt; ++j) {
-        const int gg = gt + j, sb = gg & 1;
+        const int gg = gt + j, sb = gg % NS;
         // tcgen05.ld/st below are warp-collective: every branch around them is warp-uniform
-        ok = __all_sync(0xffffffffu, tc::mbar_wait<SW>(bar(V_SFULL + sb), (gg >> 1) & 1, wait_ns, s_abort));
+        ok = __all_sync(0xffffffffu, tc::mbar_wait<SW>(bar(V_SFULL + sb), (gg / NS) & 1, wait_ns, s_abort));
         if (!ok) break;
         tc::tc_fence_after();
         const uint32_t tS = tmem + t_lane + sb * BN;
@@ -590,7 +637,10 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
           m_used = (mx == -INFINITY) ? 0.f : mx;
         } else if (__any_sync(0xffffffffu, grow)) {
           // PV of the previous tile must have landed in O before it is rescaled
-          ok = __all_sync(0xffffffffu, tc::mbar_wait<SW>(bar(V_PVDONE), (gg - 1) & 1, wait_ns, s_abort));
+          // (one barrier per S buffer: up to NS - 1 PVs may be in flight, but
+          // only the one of tile gg - 1 on its buffer's barrier)
+          ok = __all_sync(0xffffffffu, tc::mbar_wait<SW>(bar(V_PVDONE + (gg - 1) % NS), ((gg - 1) / NS) & 1,
+                                                          wait_ns, s_abort));
           if (!ok) break;
           tc::tc_fence_after();
           const float m_new = grow ? mx : m_used;
@@ -640,10 +690,11 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         if (lane == 0) tc::mbar_arrive(bar(V_PFULL + sb));
       }
       if (ok && nt > 0) ok = __all_sync(0xffffffffu, tc::mbar_wait<SW>(bar(V_ODONE), a & 1, wait_ns, s_abort));
-      // both softmax warps take the same path from here (named barriers below)
+      // every softmax warp takes the same path from here (named barriers below)
       if (lane == 0) s_info[2 + warp] = ok;
       asm volatile("bar.sync 1, %0;" ::"r"(SOFTMAX_THREADS) : "memory");
-      ok = s_info[2] && s_info[3];
+#pragma unroll
+      for (int w2 = 0; w2 < C::SM_WARPS; ++w2) ok = ok && s_info[2 + w2];
       asm volatile("bar.sync 1, %0;" ::"r"(SOFTMAX_THREADS) : "memory");
       if (!ok) {
         alive = false;
@@ -717,7 +768,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
   __syncthreads();
   if (warp == WARP_KTMA) {
     tc::tc_fence_after();
-    tc::tmem_dealloc(tmem, 256);
+    tc::tmem_dealloc(tmem, C::TMEM_COLS);
   }
   // units whose last piece this CTA held: the K/V stages are idle now and hold
   // the merge weights
@@ -726,8 +777,8 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
     __threadfence();
     for (int i = 0; i < n_merge; ++i) {
       const int u = s_merge[i];
-      merge_pieces<D>(p, u, last_cta(u, p.TM, p.W) - first_cta(u, p.TM, p.W) + 1, tid,
-                      reinterpret_cast<float*>(smem + L::K_OFF));
+      merge_pieces<D, WIDE>(p, u, last_cta(u, p.TM, p.W) - first_cta(u, p.TM, p.W) + 1, tid,
+                            reinterpret_cast<float*>(smem + L::K_OFF));
     }
   }
 }
@@ -749,7 +800,7 @@ int num_sms() {
 // Raise the kernel's dynamic shared-memory limit once per device.
 template <typename K>
 cudaError_t set_smem_once(K kernel, int bytes, int variant) {
-  static std::atomic<int> done[64][4];
+  static std::atomic<int> done[64][8];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -763,18 +814,18 @@ struct VerifyPlan {
   int TM, W, n_cta, P_max;
 };
 
-// Partition.  Two CTAs are resident per SM.  When the units alone fill more
+// Partition.  Two CTAs (WIDE: one) are resident per SM.  When the units alone fill more
 // than half of that wave, each CTA takes one whole unit; otherwise the
 // units' tiles are spread over at most one wave, each CTA taking at least
 // MIN_SHARE tiles and at most MAX_PIECES - 2 whole units' worth (so its
 // share has at most MAX_PIECES pieces), every unit in at most MAX_SPLITS
 // pieces, no CTA empty.
-VerifyPlan verify_plan(const Geom& g, int RH) {
+VerifyPlan verify_plan(const Geom& g, int RH, bool wide) {
   VerifyPlan pl;
   const long long units = (long long)g.C * g.Hkv * RH;
   pl.TM = (g.n_visual() + g.tail_cap + BN - 1) / BN;
   const long long total = units * pl.TM;
-  const long long slots = 2LL * num_sms();
+  const long long slots = (long long)(wide ? VCfg<true>::CTAS_PER_SM : VCfg<false>::CTAS_PER_SM) * num_sms();
   if (units <= slots && 2 * units > slots) {
     // one whole unit per CTA already fills most of the wave: no partials
     pl.W = pl.TM;
@@ -803,19 +854,26 @@ bool all_single(const VerifyPlan& pl, long long units) {
 
 }  // namespace
 
-// Block rows per kv head in units of at most MAX_ROWS: each (cache, kv head,
-// row half) is one work unit that streams the plane's keys.
-int row_halves(int Hq, int Hkv, int blk) { return (blk * (Hq / Hkv) + MAX_ROWS - 1) / MAX_ROWS; }
+// The WIDE form serves blocks of more than 64 rows per kv head.
+bool verify_wide(int Hq, int Hkv, int blk) { return blk * (Hq / Hkv) > VCfg<false>::ROWS; }
+
+// Block rows per kv head in units of at most ROWS of the form: each (cache,
+// kv head, row unit) is one work unit that streams the plane's keys.
+int row_halves(int Hq, int Hkv, int blk) {
+  const int rows = verify_wide(Hq, Hkv, blk) ? VCfg<true>::ROWS : VCfg<false>::ROWS;
+  return (blk * (Hq / Hkv) + rows - 1) / rows;
+}
 
 // Workspace: [units] int32 counters (256-byte aligned block), then the fp32
 // partial O rows and the (m, l) pairs of units x P_max piece slots, each slot
-// holding a unit's (at most MAX_ROWS) rows.
+// holding a unit's (at most ROWS of the form) rows.
 size_t verify_ws_bytes(const Geom& g, int Hq, int blk) {
+  const bool wide = verify_wide(Hq, g.Hkv, blk);
   const int RH = row_halves(Hq, g.Hkv, blk);
-  const VerifyPlan pl = verify_plan(g, RH);
+  const VerifyPlan pl = verify_plan(g, RH, wide);
   const size_t units = (size_t)g.C * g.Hkv * RH;
   if (units == 0 || all_single(pl, (long long)units)) return 0;
-  const size_t rows = units * pl.P_max * min(blk * (Hq / g.Hkv), MAX_ROWS);
+  const size_t rows = units * pl.P_max * min(blk * (Hq / g.Hkv), wide ? VCfg<true>::ROWS : VCfg<false>::ROWS);
   return (units * 4 + 255) / 256 * 256 + rows * (g.d + 2) * sizeof(float);
 }
 
@@ -827,7 +885,9 @@ cudaError_t launch_verify_tc(const Geom& g, int Hq, int blk, const int32_t* tail
                              const void* k, const void* vt, const float* rope, const int32_t* head,
                              void* ws, size_t ws_bytes, float sm_scale, int32_t* status, uint64_t wait_ns,
                              cudaStream_t st) {
-  if (g.V > MAX_VIEWS || Hq / g.Hkv > MAX_ROWS) return cudaErrorNotSupported;
+  const bool wide = verify_wide(Hq, g.Hkv, blk);
+  const int ROWS = wide ? VCfg<true>::ROWS : VCfg<false>::ROWS;
+  if (g.V > MAX_VIEWS || Hq / g.Hkv > VCfg<false>::ROWS) return cudaErrorNotSupported;
   const int RH = row_halves(Hq, g.Hkv, blk);
   const size_t units = (size_t)g.C * g.Hkv * RH;
   if (units == 0) return cudaSuccess;
@@ -839,7 +899,7 @@ cudaError_t launch_verify_tc(const Geom& g, int Hq, int blk, const int32_t* tail
     // G heads of one kv head for the tokens of one row half, i.e. its block
     // rows (token, head)
     const int G = Hq / g.Hkv;
-    const int box_tok = RH > 1 ? MAX_ROWS / G : blk;
+    const int box_tok = RH > 1 ? ROWS / G : blk;
     cuuint64_t dims[3] = {(cuuint64_t)g.d, (cuuint64_t)Hq, (cuuint64_t)g.C * blk};
     cuuint64_t strides[2] = {(cuuint64_t)g.d * 2, (cuuint64_t)Hq * g.d * 2};
     cuuint32_t box[3] = {64, (cuuint32_t)G, (cuuint32_t)box_tok};
@@ -851,7 +911,7 @@ cudaError_t launch_verify_tc(const Geom& g, int Hq, int blk, const int32_t* tail
            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
-  const VerifyPlan pl = verify_plan(g, RH);
+  const VerifyPlan pl = verify_plan(g, RH, wide);
   VerifyParams p;
   p.g = g;
   p.Hq = Hq;
@@ -859,8 +919,8 @@ cudaError_t launch_verify_tc(const Geom& g, int Hq, int blk, const int32_t* tail
   p.blk = blk;
   p.R = blk * p.G;
   p.RH = RH;
-  p.RU = min(p.R, MAX_ROWS);
-  p.TQH = RH > 1 ? MAX_ROWS / p.G : blk;
+  p.RU = min(p.R, ROWS);
+  p.TQH = RH > 1 ? ROWS / p.G : blk;
   p.TM = pl.TM;
   p.W = pl.W;
   p.P_max = pl.P_max;
@@ -886,7 +946,7 @@ cudaError_t launch_verify_tc(const Geom& g, int Hq, int blk, const int32_t* tail
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.gridDim = dim3((unsigned)pl.n_cta);
-  cfg.blockDim = dim3(NTHREADS);
+  cfg.blockDim = dim3(wide ? VCfg<true>::NT : VCfg<false>::NT);
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
@@ -897,12 +957,20 @@ cudaError_t launch_verify_tc(const Geom& g, int Hq, int blk, const int32_t* tail
     cfg.dynamicSmemBytes = smem;
     return cudaLaunchKernelEx(&cfg, kernel, tk, tv, tq, p);
   };
-  if (g.d == 128)
-    e = sw ? launch(verify_tc_kernel<128, true>, VLayout<128>::ALLOC, 2)
-           : launch(verify_tc_kernel<128, false>, VLayout<128>::ALLOC, 0);
-  else
-    e = sw ? launch(verify_tc_kernel<64, true>, VLayout<64>::ALLOC, 3)
-           : launch(verify_tc_kernel<64, false>, VLayout<64>::ALLOC, 1);
+  if (wide) {
+    if (g.d == 128)
+      e = sw ? launch(verify_tc_kernel<128, true, true>, VLayout<128, true>::ALLOC, 6)
+             : launch(verify_tc_kernel<128, false, true>, VLayout<128, true>::ALLOC, 4);
+    else
+      e = sw ? launch(verify_tc_kernel<64, true, true>, VLayout<64, true>::ALLOC, 7)
+             : launch(verify_tc_kernel<64, false, true>, VLayout<64, true>::ALLOC, 5);
+  } else if (g.d == 128) {
+    e = sw ? launch(verify_tc_kernel<128, true, false>, VLayout<128, false>::ALLOC, 2)
+           : launch(verify_tc_kernel<128, false, false>, VLayout<128, false>::ALLOC, 0);
+  } else {
+    e = sw ? launch(verify_tc_kernel<64, true, false>, VLayout<64, false>::ALLOC, 3)
+           : launch(verify_tc_kernel<64, false, false>, VLayout<64, false>::ALLOC, 1);
+  }
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 

@@ -119,12 +119,13 @@ def test_call_arguments_are_checked(L):
     ws = L.skv_verify_workspace_bytes(r, 32, 9)
     args = [p(FAKE)] * 5
     # block too large for the tail; more than 64 query heads per kv head; a
-    # block of more than 64 rows per kv head whose group size does not divide
-    # 64 (rows are taken 64 at a time, whole tokens each); ids half given
+    # block of more than 128 rows per kv head whose group size does not divide
+    # 128 (rows are taken 128 at a time, whole tokens each); ids half given
     assert L.stream_attn_verify(r, 32, 129, *args, None, None, None, None, p(FAKE), ws, 1.0, None) == skv.SKV_ERR_INVALID
     assert L.stream_attn_verify(r, 1024, 9, *args, None, None, None, None, p(FAKE), ws, 1.0, None) == skv.SKV_ERR_UNSUPPORTED
-    assert L.stream_attn_verify(r, 24, 22, *args, None, None, None, None, p(FAKE), ws, 1.0, None) == skv.SKV_ERR_UNSUPPORTED
-    assert L.stream_attn_verify(r, 24, 21, *args, None, None, None, None, p(FAKE), ws, 1.0, None) != skv.SKV_ERR_UNSUPPORTED
+    assert L.stream_attn_verify(r, 24, 43, *args, None, None, None, None, p(FAKE), ws, 1.0, None) == skv.SKV_ERR_UNSUPPORTED
+    assert L.stream_attn_verify(r, 24, 42, *args, None, None, None, None, p(FAKE), ws, 1.0, None) != skv.SKV_ERR_UNSUPPORTED
+    assert L.stream_attn_verify(r, 24, 22, *args, None, None, None, None, p(FAKE), ws, 1.0, None) != skv.SKV_ERR_UNSUPPORTED
     assert L.stream_attn_verify(r, 32, 9, *args, p(FAKE), p(FAKE), None, p(FAKE), p(FAKE), ws, 1.0, None) == skv.SKV_ERR_INVALID
     assert L.stream_attn_verify(r, 32, 0, *args, None, None, None, None, p(FAKE), ws, 1.0, None) == skv.SKV_ERR_INVALID
 

@@ -227,8 +227,8 @@ def test_verify_large_tail_capacity_uneven_tails(B):
 @pytest.mark.parametrize("B", [1, 8, 64])
 def test_verify_17_query_block(B):
     """A 17-query block (the last accepted token + 16 drafts): 68 block rows
-    per kv head, taken as two row halves (64 + 4) that each stream the plane's
-    keys; accept lengths up to 16."""
+    per kv head, one unit of the 128-row form that streams each plane's keys
+    once; accept lengths up to 16."""
     w = W["alpamayo_verify"].with_(C=B, blk=17)
     watch = list(range(B)) if B <= 8 else [0, 1, 31, 62, 63]
     pair = Pair(w, "b17_%d" % B, watch=watch)
@@ -254,8 +254,8 @@ def test_verify_17_query_block(B):
 
 # Degenerate and ragged geometries: no prefix, one view of one frame,
 # one-token frames, MHA (G = 1), eight query heads per kv head (a 9-query
-# block is then 72 rows: two row halves), frames and prefixes that fill no
-# tile evenly.
+# block is then 72 rows: one unit of the 128-row form), frames and prefixes
+# that fill no tile evenly.
 DEGENERATE = [
     # name, P, V, F, T, Hq, Hkv, d
     ("no_prefix", 0, 2, 3, 40, 8, 2, 64),
@@ -285,6 +285,45 @@ def test_degenerate_geometries(geo):
     for c in range(w.C):
         want, _ = O.stream_verify(pair.win[c], q[c], k[c], v[c], w.theta, w.sm_scale)
         assert_close(got[c], want, "%s verify cache %d" % (name, c))
+    assert pair.cache.device_status() == 0
+
+
+WIDE_BLOCKS = [
+    # name, Hq, Hkv, d, blk: rows per kv head = blk * Hq / Hkv
+    ("d64_68_rows", 8, 2, 64, 17),       # head_dim 64: one key row per RoPE thread
+    ("g8_136_rows", 64, 8, 128, 17),     # two units of the 128-row form per plane
+    ("g4_128_rows", 32, 8, 128, 32),     # exactly one full unit
+]
+
+
+@pytest.mark.parametrize("geo", WIDE_BLOCKS, ids=[g[0] for g in WIDE_BLOCKS])
+def test_verify_blocks_of_more_than_64_rows(geo):
+    """Blocks of more than 64 rows per kv head run on the 128-row form of the
+    verify kernel; uneven tails, every block row against the oracle."""
+    name, Hq, Hkv, d, blk = geo
+    w = synth.Workload(name, P=12, V=2, F=2, T=50, Hq=Hq, Hkv=Hkv, d=d, theta=1e4, C=3,
+                       sm_scale=1.0 / np.sqrt(d), tail_cap=96, tail_len=5, blk=blk)
+    pair = Pair(w, "wd")
+    pair.fill()
+    pair.insert()
+    tails = [0, 23, 51]
+    tk, tv = synth.tail_kv(w, max(tails), pair.tag)
+    skv.kv_write_rows(pair.cache, pair.cache.n_visual, to_dev(tk), to_dev(tv))
+    for c in range(w.C):
+        pair.win[c].set_tail(tk[c][:tails[c]], tv[c][:tails[c]])
+    q, k, v = synth.verify_block(w, pair.tag)
+    target, draft, planted = synth.planted_ids(w.C, w.blk, pair.tag)
+    tail = torch.tensor(tails, dtype=torch.int32, device="cuda")
+    out, acc, nxt = skv.stream_attn_verify(
+        pair.cache, tail, to_dev(q), to_dev(k), to_dev(v), w.sm_scale,
+        target_ids=torch.from_numpy(target).cuda(), draft_ids=torch.from_numpy(draft).cuda())
+    got = bf16_dev_to_f64(out)
+    acc, nxt = acc.cpu().numpy(), nxt.cpu().numpy()
+    for c in range(w.C):
+        want, _ = O.stream_verify(pair.win[c], q[c], k[c], v[c], w.theta, w.sm_scale)
+        assert_close(got[c], want, "%s verify cache %d (tail %d)" % (name, c, tails[c]))
+        a, n = O.accept_length(target[c], draft[c])
+        assert acc[c] == a == planted[c] and nxt[c] == n
     assert pair.cache.device_status() == 0
 
 
