@@ -235,32 +235,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
   const int zc = c * g.Hkv + h;                    // (cache, kv head) plane of the tensor maps
   const uint64_t wait_ns = p.wait_ns;
 
-  // The query tiles depend on nothing the set-up computes: their copy starts
-  // at entry (its barrier is initialised here, the others below).  Both
-  // tiles: rows (token, head) of kv head h, 64 columns per box.
-  if (warp == WARP_KTMA && lane == 0) {
-    tc::mbar_init(bar(B_QLOAD), 1);
-    tc::fence_barrier_init();
-    tc::fence_proxy_async_smem();
-    tc::prefetch_tmap(&tmap_q);
-    const int z0 = c * p.NQ + qoff + t0;
-    tc::mbar_arrive_expect_tx(bar(B_QLOAD), 2 * L::QT);
-#pragma unroll
-    for (int i = 0; i < 2; ++i)
-#pragma unroll
-      for (int hf = 0; hf < D / 64; ++hf)
-        tc::tma_load_3d(sbase + L::Q_OFF + i * L::QT + hf * L::HALF_Q, &tmap_q, bar(B_QLOAD), hf * 64, h * p.G,
-                        z0 + i * p.TQ);
-  }
-
-  // The copies of key tile j into stage j % NST: this CTA's 64 K rows (K
-  // producer) or its D/2 V^T rows of the 128 keys (V producer).  A 64-row
-  // block of a view's new frame comes from the step's input [C][V][T][Hkv][d]
-  // when the insert is fused: K rows as they are, V token-major (an MN-major
-  // operand for the PV product); every other block from the ring.
-  auto issue_tile = [&](bool is_k, int j) {
-    const int s = j % NST, r0 = s_tiles[j];
-    const uint32_t src = FUSED ? s_src[j] : 0u;
+  // The copies of a key tile (first row r0, new-frame flags src) into stage
+  // s: this CTA's 64 K rows (K producer) or its D/2 V^T rows of the 128 keys
+  // (V producer).  A 64-row block of a view's new frame comes from the
+  // step's input [C][V][T][Hkv][d] when the insert is fused: K rows as they
+  // are, V token-major (an MN-major operand for the PV product); every other
+  // block from the ring.
+  auto issue_rows = [&](bool is_k, int s, int r0, uint32_t src) {
     auto new_block = [&](int r, int& t_in, int& cv) {
       const int u = r - g.P, v = u / FT;
       t_in = u % FT % g.T;
@@ -297,11 +278,60 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
       }
     }
   };
+  auto issue_tile = [&](bool is_k, int j) { issue_rows(is_k, j % NST, s_tiles[j], FUSED ? s_src[j] : 0u); };
+
+  // With a prefix of at least one key tile, every item's first tile is rows
+  // [0, BN): prefix keys, which every query sees (no hole reaches them) and
+  // no new frame holds.  Its copies start at entry too, with the queries'.
+  const bool early0 = g.P >= BN;
+
+  // RoPE warps: R(1) of their chunk and, with early0, the first-row angles of
+  // tile 0 (a prefix row: its position is its row), loaded at entry
+  float4 e_step4[4], e_pf[4];
+  if (warp >= WARP_ROPE) {
+    const int rt = tid - WARP_ROPE * 32, ln = rt & 31;
+    constexpr int HALF = D / 2, NCH = HALF / 8, NPT = HN * NCH / 128;
+    const int ea = (ln % NCH) * 8;
+    const int row0 = HN * (int)rank + (rt >> 5) * (HN / 4) + (ln / NCH) * NPT;
+    const float4* rope4 = reinterpret_cast<const float4*>(p.rope);
+#pragma unroll
+    for (int w4 = 0; w4 < 4; ++w4) e_step4[w4] = __ldg(rope4 + (HALF + ea) / 2 + w4);
+    if (early0) {
+#pragma unroll
+      for (int w4 = 0; w4 < 4; ++w4) e_pf[w4] = __ldg(rope4 + ((size_t)row0 * HALF + ea) / 2 + w4);
+    }
+  }
+
+  // The query tiles depend on nothing the set-up computes: their copy starts
+  // at entry (its barrier is initialised here, the others below).  Both
+  // tiles: rows (token, head) of kv head h, 64 columns per box.
+  if ((warp == WARP_KTMA || warp == WARP_VTMA) && lane == 0 && early0) {
+    const bool is_k = warp == WARP_KTMA;
+    tc::mbar_init(bar(is_k ? B_KFULL : B_VFULL), 1);
+    tc::fence_barrier_init();
+    tc::fence_proxy_async_smem();
+    tc::prefetch_tmap(is_k ? &tmap_k : &tmap_v);
+    issue_rows(is_k, 0, 0, 0u);
+  }
+  if (warp == WARP_KTMA && lane == 0) {
+    tc::mbar_init(bar(B_QLOAD), 1);
+    tc::fence_barrier_init();
+    tc::fence_proxy_async_smem();
+    tc::prefetch_tmap(&tmap_q);
+    const int z0 = c * p.NQ + qoff + t0;
+    tc::mbar_arrive_expect_tx(bar(B_QLOAD), 2 * L::QT);
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+#pragma unroll
+      for (int hf = 0; hf < D / 64; ++hf)
+        tc::tma_load_3d(sbase + L::Q_OFF + i * L::QT + hf * L::HALF_Q, &tmap_q, bar(B_QLOAD), hf * 64, h * p.G,
+                        z0 + i * p.TQ);
+  }
 
   if (warp == 0) {
     if (lane == 0) {
       for (int i = 0; i < B_COUNT; ++i) {
-        if (i == B_QLOAD) continue;
+        if (i == B_QLOAD || (early0 && (i == B_KFULL || i == B_VFULL))) continue;
         // warpgroup-wide events arrive once per warp (after __syncwarp)
         int count = 1;
         if (i == B_PFULL || i == B_PFULL + 1) count = 8;      // 2 CTAs x 4 warps
@@ -380,7 +410,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
     if (lane == 0) {
       const int n0 = *s_ntiles;
       tc::prefetch_tmap(warp == WARP_KTMA ? &tmap_k : &tmap_v);
-      for (int j = 0; j < n0 && j < NST; ++j) issue_tile(warp == WARP_KTMA, j);
+      for (int j = early0 ? 1 : 0; j < n0 && j < NST; ++j) issue_tile(warp == WARP_KTMA, j);
     }
   }
   if (warp == WARP_KTMA) {
@@ -415,8 +445,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
       // -------------------------------------- producers of this CTA's halves
       const bool is_k = warp == WARP_KTMA;
       if (lane == 0) {
-        // tiles [0, NST) were issued before the cluster barrier
-        int issued = min(nt, NST);
+        // tiles [0, NST) were issued before the cluster barrier (tile 0 at
+        // entry with early0, even for an item that then has no tiles)
+        int issued = max(min(nt, NST), early0 ? 1 : 0);
         for (int j = NST; j < nt; ++j) {
           const int s = j % NST, u = j / NST;
           if (!tc::mbar_wait_cluster<SW>(bar((is_k ? B_KEMPTY : B_VEMPTY) + s), (u - 1) & 1, wait_ns, s_abort))
@@ -587,10 +618,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
     const uint32_t off_a = (ea / 64) * L::HALF_K, off_b = (eb / 64) * L::HALF_K;
     const int ca = (ea % 64) / 8, cb = (eb % 64) / 8;
     const float4* rope4 = reinterpret_cast<const float4*>(p.rope);
-    float4 step4[4];
-#pragma unroll
-    for (int w4 = 0; w4 < 4; ++w4) step4[w4] = __ldg(rope4 + (HALF + ea) / 2 + w4);   // R(1)
-    const Ang8 step = ang8_from(step4);
+    const Ang8 step = ang8_from(e_step4);             // R(1), loaded at entry
     const int row0 = HN * (int)rank + row_base;       // this thread's first row inside a tile
     int pf_pos = -1, pf_run = 0;
     float4 pf[4];
@@ -603,7 +631,18 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
         for (int w4 = 0; w4 < 4; ++w4) pf[w4] = __ldg(rope4 + ((size_t)pf_pos * HALF + ea) / 2 + w4);
       }
     };
-    if (nt > 0) fetch(0);
+    if (nt > 0) {
+      if (early0 && row0 < row_end) {
+        // tile 0 is rows [0, BN) of the prefix: position = row, the rest of
+        // the prefix is its run
+        pf_pos = row0;
+        pf_run = g.rope_steps ? g.P - row0 : 1;
+#pragma unroll
+        for (int w4 = 0; w4 < 4; ++w4) pf[w4] = e_pf[w4];
+      } else {
+        fetch(0);
+      }
+    }
 #pragma unroll 1
     for (int j = 0; j < nt; ++j) {
       const int s = j % NST, u = j / NST;
@@ -656,6 +695,34 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
     const uint32_t mask_sa = sbase + L::MASK_OFF + 4u * (i * BM + row);
     int a1 = 0, n1 = 0;
     const bool wrap = *s_wrap != 0;
+    // Query rotation, part 1: the table entries of the thread's rows, loaded
+    // first (they depend only on the rows' positions, so their latency runs
+    // under the mask set-up and the queries' copy).  Query tiles as TMA
+    // landed them: bf16 row r of tile qi = (token t0 + qi*TQ + r/G, head
+    // r%G); thread tid takes chunk ch (8 frequencies) of NCH consecutive rows.
+    // Rows of one token (its G heads) share one load; the rows that reuse
+    // the previous row's entries (bit q of dup) take them once they landed.
+    constexpr int HALF = D / 2, NCH = HALF / 8;
+    const int ch = tid % NCH, rr0 = (tid / NCH) * NCH;
+    const int ea = ch * 8, eb = HALF + ch * 8;
+    float4 cs[NCH][4];
+    uint32_t dup = 0;
+    if (nt > 0) {
+      const float4* rope4 = reinterpret_cast<const float4*>(p.rope);
+      int prev_tok = -1;
+#pragma unroll
+      for (int q = 0; q < NCH; ++q) {
+        const int rr = rr0 + q, qi = rr >> 7, r = rr & 127;
+        const int qtok = min(t0 + qi * p.TQ + r / p.G, n_seg - 1);
+        if (q > 0 && qtok == prev_tok) {
+          dup |= 1u << q;
+        } else {
+#pragma unroll
+          for (int w4 = 0; w4 < 4; ++w4) cs[q][w4] = __ldg(rope4 + ((size_t)(pos0 + qtok) * HALF + ea) / 2 + w4);
+        }
+        prev_tok = qtok;
+      }
+    }
     if (nt > 0) {
       const int tq = min(tok, n_seg - 1);
       int a2 = 0, n2 = 0;
@@ -676,36 +743,18 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
     float m_used = -INFINITY, l = 0.f;
     bool ok = true;
     if (nt > 0) {
-      // query tiles as TMA landed them: bf16 row r of tile qi = (token
-      // t0 + qi*TQ + r/G, head r%G); rotate in place, at each token's
-      // logical position, into fp16.  Thread tid takes chunk ch (8
-      // frequencies) of NCH consecutive rows, four rows at a time.
-      constexpr int HALF = D / 2, NCH = HALF / 8;
-      const int ch = tid % NCH, rr0 = (tid / NCH) * NCH;
-      const int ea = ch * 8, eb = HALF + ch * 8;
+      // part 2: rotate in place, at each token's logical position, into fp16,
+      // four rows at a time
       const uint32_t off_a = (ea / 64) * L::HALF_Q, off_b = (eb / 64) * L::HALF_Q;
       const int ca = (ea % 64) / 8, cb = (eb % 64) / 8;
-      const float4* rope4 = reinterpret_cast<const float4*>(p.rope);
-      // the table entries of every row first: they depend only on the rows'
-      // positions, so their loads overlap the queries' copy.  Rows of one
-      // token (its G heads) share them: one load per token.
-      float4 cs[NCH][4];
-      int prev_tok = -1;
-#pragma unroll
-      for (int q = 0; q < NCH; ++q) {
-        const int rr = rr0 + q, qi = rr >> 7, r = rr & 127;
-        const int qtok = min(t0 + qi * p.TQ + r / p.G, n_seg - 1);
-        if (q > 0 && qtok == prev_tok) {
-#pragma unroll
-          for (int w4 = 0; w4 < 4; ++w4) cs[q][w4] = cs[q - 1][w4];
-        } else {
-#pragma unroll
-          for (int w4 = 0; w4 < 4; ++w4) cs[q][w4] = __ldg(rope4 + ((size_t)(pos0 + qtok) * HALF + ea) / 2 + w4);
-        }
-        prev_tok = qtok;
-      }
       ok = __all_sync(0xffffffffu, tc::mbar_wait<SW>(bar(B_QLOAD), 0, wait_ns, s_abort));
       if (ok) {
+#pragma unroll
+        for (int q = 1; q < NCH; ++q)
+          if ((dup >> q) & 1u) {
+#pragma unroll
+            for (int w4 = 0; w4 < 4; ++w4) cs[q][w4] = cs[q - 1][w4];
+          }
 #pragma unroll
         for (int b4 = 0; b4 < NCH; b4 += 4) {
           uint4 xa[4], xb[4];
