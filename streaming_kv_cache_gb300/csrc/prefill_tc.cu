@@ -166,7 +166,8 @@ __device__ __forceinline__ void ring_hole(const Geom& g, int v, int f, int slot,
 
 // FUSED: the frame insert is done by this launch (see PrefillParams): the new
 // frames' K and V come from the step's input through tmap_kn / tmap_vn.
-template <int D, bool SW, bool FUSED>
+// TABLE: rope_mode 1 (a table row per key), see rotate_key_rows.
+template <int D, bool SW, bool FUSED, bool TABLE = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                   const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_kn,
@@ -668,7 +669,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
         break;
       }
       if (pf_pos >= 0)
-        rotate_key_rows<NPT>(smem + L::K_OFF + s * L::KST, off_a, off_b, ca, cb, row_base, s_tiles[j] + row0,
+        rotate_key_rows<NPT, TABLE>(smem + L::K_OFF + s * L::KST, off_a, off_b, ca, cb, row_base, s_tiles[j] + row0,
                              row_end, pf_pos, pf_run, pf, step, g, s_head, rope4, ea, HALF);
       tc::fence_proxy_async();
       __syncwarp();
@@ -929,7 +930,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
 // largest carve-out made the 36-layer call 3% slower).
 template <typename K>
 cudaError_t set_smem_once(K kernel, int bytes, int variant) {
-  static std::atomic<int> done[64][6];
+  static std::atomic<int> done[64][7];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -1079,6 +1080,8 @@ cudaError_t launch_prefill_tc(const Geom& g, int Hq, const PrefillQuery& qs, con
   if (fused)
     e = sw ? launch(prefill_tc_kernel<128, true, true>, Layout<128>::ALLOC, 5)
            : launch(prefill_tc_kernel<128, false, true>, Layout<128>::ALLOC, 4);
+  else if (g.d == 128 && !sw && !g.rope_steps)
+    e = launch(prefill_tc_kernel<128, false, false, true>, Layout<128>::ALLOC, 6);
   else if (g.d == 128)
     e = sw ? launch(prefill_tc_kernel<128, true, false>, Layout<128>::ALLOC, 2)
            : launch(prefill_tc_kernel<128, false, false>, Layout<128>::ALLOC, 0);

@@ -110,7 +110,10 @@ __device__ __forceinline__ void rotate8(uint4& a, uint4& b, const Ang8& t) {
 // first describe row r0 (its logical position, the rows from it on with
 // consecutive positions, its table angles).  Inside one run the angles step
 // by R(1); rows are loaded two at a time before they are rotated.
-template <int NPT>
+// TABLE: compiled for a table row per key (rope_mode 1); the kernels that
+// take it are instantiated for that mode alone, so the stepping path of the
+// others keeps its registers.
+template <int NPT, bool TABLE = false>
 __device__ __forceinline__ void rotate_key_rows(uint8_t* kt, uint32_t off_a, uint32_t off_b, int ca, int cb,
                                                 int row_base, int r0, int row_lim, int pos, int run,
                                                 const float4 (&first)[4], const Ang8& step, const Geom& g,
@@ -134,6 +137,28 @@ __device__ __forceinline__ void rotate_key_rows(uint8_t* kt, uint32_t off_a, uin
         *reinterpret_cast<uint4*>(kt + off_a + tc::sw128_off(row_base + k0 + k, ca)) = xa[k];
         *reinterpret_cast<uint4*>(kt + off_b + tc::sw128_off(row_base + k0 + k, cb)) = xb[k];
       }
+    }
+    return;
+  }
+  if (TABLE && !g.rope_steps && r0 + NPT <= row_lim) {
+    // a table row per key (no stepping): the loads of every row after the
+    // first go out together, then the rows are rotated
+    float4 t[NPT > 1 ? NPT - 1 : 1][4];
+#pragma unroll
+    for (int k = 1; k < NPT; ++k) {
+      int pk, rk;
+      key_pos_run(g, heads, r0 + k, pk, rk);
+#pragma unroll
+      for (int w4 = 0; w4 < 4; ++w4) t[k - 1][w4] = __ldg(rope4 + ((size_t)pk * half + ea) / 2 + w4);
+    }
+#pragma unroll
+    for (int k = 0; k < NPT; ++k) {
+      uint4* pa = reinterpret_cast<uint4*>(kt + off_a + tc::sw128_off(row_base + k, ca));
+      uint4* pb = reinterpret_cast<uint4*>(kt + off_b + tc::sw128_off(row_base + k, cb));
+      uint4 xa = *pa, xb = *pb;
+      rotate8(xa, xb, k == 0 ? ang8_from(first) : ang8_from(t[k > 0 ? k - 1 : 0]));
+      *pa = xa;
+      *pb = xb;
     }
     return;
   }

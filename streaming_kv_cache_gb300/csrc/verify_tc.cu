@@ -260,7 +260,8 @@ __device__ __noinline__ void merge_pieces(const VerifyParams& p, int u, int n, i
 }
 
 // SW: compiled for a wait limit under the suspend hint (see tc::bounded_wait)
-template <int D, bool SW, bool WIDE>
+// TABLE: rope_mode 1 (a table row per key), see rotate_key_rows.
+template <int D, bool SW, bool WIDE, bool TABLE = false>
 __global__ void __launch_bounds__(VCfg<WIDE>::NT, VCfg<WIDE>::CTAS_PER_SM)
 verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                  const __grid_constant__ CUtensorMap tmap_q, const VerifyParams p) {
@@ -551,7 +552,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         const int gg = gt + j, s = gg % KST;
         if (!(ok = tc::mbar_wait<SW>(bar(V_KFULL + s), (gg / KST) & 1, wait_ns, s_abort))) break;
         if (pf_pos >= 0)
-          rotate_key_rows<NPT>(smem + L::K_OFF + s * L::KT, off_a, off_b, ca, cb, row_base, (ta + j) * BN + row_base,
+          rotate_key_rows<NPT, TABLE>(smem + L::K_OFF + s * L::KT, off_a, off_b, ca, cb, row_base, (ta + j) * BN + row_base,
                                row_lim, pf_pos, pf_run, pf, step, g, s_head, rope4, ea, HALF);
         if (j + 1 < nt) {
           if (pf_pos >= 0 && pf_run > BN && (ta + j + 1) * BN + row_base < row_lim) {
@@ -800,7 +801,7 @@ int num_sms() {
 // Raise the kernel's dynamic shared-memory limit once per device.
 template <typename K>
 cudaError_t set_smem_once(K kernel, int bytes, int variant) {
-  static std::atomic<int> done[64][8];
+  static std::atomic<int> done[64][10];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -957,7 +958,11 @@ cudaError_t launch_verify_tc(const Geom& g, int Hq, int blk, const int32_t* tail
     cfg.dynamicSmemBytes = smem;
     return cudaLaunchKernelEx(&cfg, kernel, tk, tv, tq, p);
   };
-  if (wide) {
+  const bool table = g.d == 128 && !sw && !g.rope_steps;
+  if (table) {
+    e = wide ? launch(verify_tc_kernel<128, false, true, true>, VLayout<128, true>::ALLOC, 9)
+             : launch(verify_tc_kernel<128, false, false, true>, VLayout<128, false>::ALLOC, 8);
+  } else if (wide) {
     if (g.d == 128)
       e = sw ? launch(verify_tc_kernel<128, true, true>, VLayout<128, true>::ALLOC, 6)
              : launch(verify_tc_kernel<128, false, true>, VLayout<128, true>::ALLOC, 4);
