@@ -10,7 +10,8 @@
 // One CTA copies a chunk of CH tokens of one (cache, group, kv head): the K
 // rows are straight 16-byte copies into [row][d]; the V rows go through
 // shared memory and are written transposed into [d][row], one coalesced run
-// of CH tokens per dimension.
+// of CH tokens per dimension.  In a full chunk every thread has all of its
+// 16-byte loads in flight before its first store.
 //
 // The verify block's tail write also computes the greedy accept length (it
 // needs only the token ids) and lets the attention kernel that follows launch
@@ -85,14 +86,34 @@ __global__ void __launch_bounds__(THREADS) write_rows_kernel(
     const uint16_t* ks = k_src + (((size_t)c * n_group + grp) * n_tok + t0) * src_tok_stride + (size_t)h * D;
     const uint16_t* vs = v_src + (((size_t)c * n_group + grp) * n_tok + t0) * src_tok_stride + (size_t)h * D;
     uint16_t* kd = k + (((size_t)c * g.Hkv + h) * g.row_cap + base + t0) * D;
-    for (int i = threadIdx.x; i < nt * VEC; i += THREADS) {
-      const int t = i / VEC, j = i - t * VEC;
-      const uint4 val = *reinterpret_cast<const uint4*>(ks + t * src_tok_stride + j * 8);
-      *reinterpret_cast<uint4*>(kd + (size_t)t * D + j * 8) = val;
-      const uint4 vv = *reinterpret_cast<const uint4*>(vs + t * src_tok_stride + j * 8);
-      const uint16_t* pv = reinterpret_cast<const uint16_t*>(&vv);
+    constexpr int PER = CH * VEC / THREADS;   // vectors per thread of a full chunk
+    if (nt == CH) {
+      // a full chunk: every load of this thread in flight before its stores
+      uint4 kv[PER], vv[PER];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) sv[t][j * 8 + e] = pv[e];
+      for (int q = 0; q < PER; ++q) {
+        const int i = threadIdx.x + q * THREADS, t = i / VEC, j = i - t * VEC;
+        kv[q] = *reinterpret_cast<const uint4*>(ks + t * src_tok_stride + j * 8);
+        vv[q] = *reinterpret_cast<const uint4*>(vs + t * src_tok_stride + j * 8);
+      }
+#pragma unroll
+      for (int q = 0; q < PER; ++q) {
+        const int i = threadIdx.x + q * THREADS, t = i / VEC, j = i - t * VEC;
+        *reinterpret_cast<uint4*>(kd + (size_t)t * D + j * 8) = kv[q];
+        const uint16_t* pv = reinterpret_cast<const uint16_t*>(&vv[q]);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) sv[t][j * 8 + e] = pv[e];
+      }
+    } else {
+      for (int i = threadIdx.x; i < nt * VEC; i += THREADS) {
+        const int t = i / VEC, j = i - t * VEC;
+        const uint4 val = *reinterpret_cast<const uint4*>(ks + t * src_tok_stride + j * 8);
+        *reinterpret_cast<uint4*>(kd + (size_t)t * D + j * 8) = val;
+        const uint4 vv = *reinterpret_cast<const uint4*>(vs + t * src_tok_stride + j * 8);
+        const uint16_t* pv = reinterpret_cast<const uint16_t*>(&vv);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) sv[t][j * 8 + e] = pv[e];
+      }
     }
     __syncthreads();
     // V: transposed write, one run of nt tokens per dimension.
