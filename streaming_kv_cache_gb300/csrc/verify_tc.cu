@@ -73,6 +73,9 @@ struct VCfg {
   static constexpr int WARP_KTMA = SM_WARPS, WARP_VTMA = SM_WARPS + 1, WARP_MMA = SM_WARPS + 2;
   static constexpr int WARP_ROPE = WIDE ? 8 : 5;   // (WIDE: warp 7 has no role)
   static constexpr int ROPE_WARPS = WIDE ? 8 : 4;
+  // RoPE groups: the RoPE warps split into RG groups that rotate alternate
+  // key tiles (all of them rotate each piece's query block)
+  static constexpr int RG = WIDE ? 2 : 1;
   static constexpr int NT = (WARP_ROPE + ROPE_WARPS) * 32;
   static constexpr int CTAS_PER_SM = WIDE ? 1 : 2;
   // K stages (a K tile is held through its rotation) and V^T stages: one
@@ -296,7 +299,8 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
     if (lane == 0) {
       for (int i = 0; i < V_COUNT; ++i) {
         int count = 1;
-        if (i == V_QFULL || (i >= V_KROT && i < V_KROT + KST)) count = C::ROPE_WARPS;
+        if (i == V_QFULL) count = C::ROPE_WARPS;
+        if (i >= V_KROT && i < V_KROT + KST) count = C::ROPE_WARPS / C::RG;
         if ((i >= V_PFULL && i < V_PFULL + NS) || i == V_OFREE) count = C::SM_WARPS;
         tc::mbar_init(bar(i), count);
       }
@@ -471,10 +475,12 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
     const int wr = rt >> 5, ln = rt & 31;
     constexpr int HALF = D / 2;
     constexpr int NCH = HALF / 8;
-    constexpr int NPT = BN * NCH / NRT;   // key rows per thread
+    constexpr int RG = C::RG, RW = C::ROPE_WARPS / RG;   // groups of RW warps, alternate tiles
+    constexpr int NPT = BN * NCH / (RW * 32);           // key rows per thread
+    const int grp = wr / RW;
     int* s_head = reinterpret_cast<int*>(smem + L::HEAD_OFF) + wr * MAX_VIEWS;   // this warp's copy
     const int ch = ln % NCH;
-    const int row_base = wr * (BN / C::ROPE_WARPS) + (ln / NCH) * NPT;
+    const int row_base = (wr % RW) * (BN / RW) + (ln / NCH) * NPT;
     const int ea = ch * 8, eb = HALF + ch * 8;
     const uint32_t off_a = (ea / 64) * L::HALF_K, off_b = (eb / 64) * L::HALF_K;
     const int ca = (ea % 64) / 8, cb = (eb % 64) / 8;
@@ -483,12 +489,13 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
 #pragma unroll
     for (int w4 = 0; w4 < 4; ++w4) step4[w4] = __ldg(rope4 + (HALF + ea) / 2 + w4);   // R(1)
     const Ang8 step = ang8_from(step4);
-    // R(BN) of every chunk in this warp's shared memory: a thread's first row
-    // of the next tile, BN rows on inside the same run, is this tile's first
-    // row turned by R(BN), no table load
+    // R(RG BN) of every chunk in this warp's shared memory: a thread's first
+    // row of its group's next tile, RG BN rows on inside the same run, is
+    // this tile's first row turned by R(RG BN), no table load
     float4* s_r64 = reinterpret_cast<float4*>(smem + L::R64_OFF) + wr * NCH * 4;
-    // (a table of at most BN rows has no run longer than BN to turn along)
-    if (ln < NCH * 4 && g.rope_len > BN) s_r64[ln] = __ldg(rope4 + ((size_t)BN * HALF + (ln / 4) * 8) / 2 + ln % 4);
+    // (a table of at most RG BN rows has no run longer than that to turn along)
+    if (ln < NCH * 4 && g.rope_len > RG * BN)
+      s_r64[ln] = __ldg(rope4 + ((size_t)(RG * BN) * HALF + (ln / 4) * 8) / 2 + ln % 4);
     __syncwarp();
     int gt = 0, a = 0;
     bool ok = true, q_in_flight = false;
@@ -546,16 +553,19 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
           for (int w4 = 0; w4 < 4; ++w4) pf[w4] = __ldg(rope4 + ((size_t)pf_pos * HALF + ea) / 2 + w4);
         }
       };
-      fetch(0);
+      // this group's tiles of the piece: j = j0, j0 + RG, ... (tile gg of the
+      // CTA belongs to group gg mod RG)
+      const int j0 = (grp - gt % RG + RG) % RG;
+      if (j0 < nt) fetch(j0);
 #pragma unroll 1
-      for (int j = 0; j < nt; ++j) {
+      for (int j = j0; j < nt; j += RG) {
         const int gg = gt + j, s = gg % KST;
         if (!(ok = tc::mbar_wait<SW>(bar(V_KFULL + s), (gg / KST) & 1, wait_ns, s_abort))) break;
         if (pf_pos >= 0)
           rotate_key_rows<NPT, TABLE>(smem + L::K_OFF + s * L::KT, off_a, off_b, ca, cb, row_base, (ta + j) * BN + row_base,
                                row_lim, pf_pos, pf_run, pf, step, g, s_head, rope4, ea, HALF);
-        if (j + 1 < nt) {
-          if (pf_pos >= 0 && pf_run > BN && (ta + j + 1) * BN + row_base < row_lim) {
+        if (j + RG < nt) {
+          if (pf_pos >= 0 && pf_run > RG * BN && (ta + j + RG) * BN + row_base < row_lim) {
             const float4* r = s_r64 + ch * 4;
 #pragma unroll
             for (int w4 = 0; w4 < 4; ++w4) {
@@ -563,10 +573,10 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
               pf[w4] = make_float4(c.x * t.x - c.y * t.y, c.y * t.x + c.x * t.y,
                                    c.z * t.z - c.w * t.w, c.w * t.z + c.z * t.w);
             }
-            pf_pos += BN;
-            pf_run -= BN;
+            pf_pos += RG * BN;
+            pf_run -= RG * BN;
           } else {
-            fetch(j + 1);
+            fetch(j + RG);
           }
         }
         tc::fence_proxy_async_smem();
