@@ -115,3 +115,22 @@ def test_mrope_alpamayo_streaming_step():
             b = w.P + v * FT + f * w.T
             rows += [b, b + 14, b + 15, b + 100, b + w.T - 1]
     _mrope_step(w, 15, "mr_a", window_rows=np.array(sorted(set(rows))))
+
+
+def test_mrope_17_token_verify_block():
+    """The multi-section reading on the 128-row form of the verify kernel
+    (17 tokens x 4 heads = 68 block rows), two caches after a ring turn."""
+    w = W["alpamayo_step"].with_(C=2, blk=17)
+    m, arg = _reading(w, 15)
+    pair = Pair(w, "mr17", mrope=arg)
+    pair.fill()
+    pair.insert()
+    bq, bk, bv = synth.verify_block(w, pair.tag)
+    tail = torch.zeros((w.C,), dtype=torch.int32, device="cuda")
+    vout, _, _ = skv.stream_attn_verify(pair.cache, tail, to_dev(bq), to_dev(bk), to_dev(bv), w.sm_scale)
+    vout = bf16_dev_to_f64(vout)
+    for c, win in pair.win.items():
+        win.set_tail(np.zeros((0, w.Hkv, w.d), np.uint16), np.zeros((0, w.Hkv, w.d), np.uint16))
+        want, _ = O.stream_verify(win, bq[c], bk[c], bv[c], w.theta, w.sm_scale, mrope=m)
+        assert_close(vout[c], want, "mrope 17-token verify cache %d" % c)
+    assert pair.cache.device_status() == 0

@@ -28,14 +28,15 @@ def _built():
     build.build()
 
 
-@pytest.mark.parametrize("name", ["tiny", "alpamayo_step"])
-def test_wait_timeout_sets_status_and_context_survives(name):
+@pytest.mark.parametrize("name,blk", [("tiny", 9), ("alpamayo_step", 9), ("alpamayo_step", 17)])
+def test_wait_timeout_sets_status_and_context_survives(name, blk):
+    """blk 17 at four query heads per kv head is 68 block rows: the 128-row
+    form of the verify kernel."""
     w = W[name] if name == "tiny" else W[name].with_(C=2)
     pair = Pair(w, "to")
     pair.fill()
     cache = pair.cache
     q = synth.frame_q(w, pair.n_inserts - 1, "to")
-    blk = 9
     wv = w.with_(blk=blk)
     qb, kb, vb = synth.verify_block(wv, "to")
     tail = torch.zeros((w.C,), dtype=torch.int32, device="cuda")
@@ -68,3 +69,28 @@ def test_wait_timeout_sets_status_and_context_survives(name):
         want, _ = O.stream_verify(pair.win[c], qb[c], kb[c], vb[c], w.theta, w.sm_scale)
         assert_close(got[c], want, "%s verify after a timeout, cache %d" % (name, c))
     assert cache.device_status() == 0
+
+
+@pytest.mark.parametrize("blk", [9, 17])
+def test_short_limit_path_matches_the_oracle(blk):
+    """A wait limit under a millisecond selects the kernels' polling
+    instantiations (no suspend hint, the clock read at every poll); with a
+    limit no wait reaches (0.9 ms) they give the same results as the normal
+    ones, for both forms of the verify kernel."""
+    w = W["alpamayo_step"].with_(C=2, blk=blk)
+    pair = Pair(w, "sl%d" % blk, wait_ns=900000)
+    pair.fill()
+    pair.insert()
+    q = synth.frame_q(w, pair.n_inserts - 1, pair.tag)
+    out = bf16_dev_to_f64(skv.stream_attn_prefill(pair.cache, to_dev(q), w.sm_scale))
+    for c in pair.watch:
+        want, _ = O.stream_prefill(pair.win[c], q[c], w.theta, w.sm_scale)
+        assert_close(out[c], want, "short-limit prefill cache %d" % c)
+    qb, kb, vb = synth.verify_block(w, pair.tag)
+    tail = torch.zeros((w.C,), dtype=torch.int32, device="cuda")
+    vout = bf16_dev_to_f64(skv.stream_attn_verify(pair.cache, tail, to_dev(qb), to_dev(kb), to_dev(vb),
+                                                  w.sm_scale)[0])
+    for c in pair.watch:
+        want, _ = O.stream_verify(pair.win[c], qb[c], kb[c], vb[c], w.theta, w.sm_scale)
+        assert_close(vout[c], want, "short-limit verify blk %d cache %d" % (blk, c))
+    assert pair.cache.device_status() == 0
