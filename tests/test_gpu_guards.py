@@ -102,9 +102,12 @@ def test_prefill_window_and_tail_write_only_their_outputs(name):
     assert pair.cache.device_status() == 0
 
 
-@pytest.mark.parametrize("name,B", [("tiny", 3), ("alpamayo_verify", 8)])
-def test_verify_writes_only_its_outputs_and_workspace(name, B):
-    w = synth.WORKLOADS[name].with_(C=B, blk=9)
+@pytest.mark.parametrize("name,B,blk", [("tiny", 3, 9), ("alpamayo_verify", 8, 9), ("alpamayo_verify", 8, 17),
+                                         ("alpamayo_verify", 1, 17)])
+def test_verify_writes_only_its_outputs_and_workspace(name, B, blk):
+    """blk 17 at four query heads per kv head runs on the 128-row form, whose
+    workspace rows per piece slot differ."""
+    w = synth.WORKLOADS[name].with_(C=B, blk=blk)
     pair = Pair(w, "guardv", watch=[])
     pair.fill()
     pair.set_tail(w.tail_len)
@@ -128,3 +131,24 @@ def test_verify_writes_only_its_outputs_and_workspace(name, B):
         assert ws_g.guards_intact(), "verify workspace: a guard band was written"
         np.testing.assert_array_equal(acc_g.t.cpu().numpy(), planted)
     assert pair.cache.device_status() == 0
+
+
+def test_fused_insert_prefill_writes_only_its_outputs():
+    """The fused insert + prefill on two caches filled alike: one writes into
+    guarded output and LSE buffers, the other into plain ones; the guards
+    hold, every element is written, and both give the same bits."""
+    w = synth.WORKLOADS["alpamayo_step"].with_(C=2)
+    pa, pb = Pair(w, "guardf", watch=[]), Pair(w, "guardf", watch=[])
+    pa.fill()
+    pb.fill()
+    k, v = (to_dev(x) for x in synth.frame_kv(w, pa.n_inserts, "guardf"))
+    q = to_dev(synth.frame_q(w, pa.n_inserts, "guardf"))
+    out_g, lse_g = Guarded(q.shape, torch.bfloat16), Guarded((w.C, w.Hq, w.n_new), torch.float32)
+    skv.stream_attn_prefill_insert(pa.cache, k, v, q, w.sm_scale, out=out_g.t, lse=lse_g.t)
+    out_p, lse_p = skv.stream_attn_prefill_insert(pb.cache, k, v, q, w.sm_scale, lse=True)
+    torch.cuda.synchronize()
+    _check_out(out_g, out_p, "fused prefill out")
+    _check_out(lse_g, lse_p, "fused prefill lse")
+    assert torch.equal(pa.cache.k, pb.cache.k) and torch.equal(pa.cache.vt, pb.cache.vt)
+    assert torch.equal(pa.cache.head, pb.cache.head)
+    assert pa.cache.device_status() == 0 and pb.cache.device_status() == 0
