@@ -64,9 +64,12 @@ constexpr int NST = 3;           // K and V stages (three ran faster than four: 
 constexpr int NTHREADS = 512;
 constexpr int WARP_KTMA = 8, WARP_MMA = 9, WARP_VFWD = 10, WARP_VTMA = 11, WARP_ROPE = 12;
 // register split (launch: 512 threads x 128): 2 x 128 x 184 + 128 x 48 + 128 x 96 = 65536
-// (measured: 184/48/96 0.8% faster than 176/56/104; 192/40/88 and 168/72/104 slower)
-constexpr int REG_SOFTMAX = 184, REG_CTRL = 48, REG_ROPE = 96;
-static_assert(256 * REG_SOFTMAX + 128 * REG_CTRL + 128 * REG_ROPE == 65536, "register split");
+// (measured: 184/48/96 0.8% faster than 176/56/104; 192/40/88 and 168/72/104 slower).
+// With the insert fused the control warps also transpose V: 176/56/104 there.
+template <bool FUSED> struct RegSplit {
+  static constexpr int SOFTMAX = FUSED ? 176 : 184, CTRL = FUSED ? 56 : 48, ROPE = FUSED ? 104 : 96;
+  static_assert(256 * SOFTMAX + 128 * CTRL + 128 * ROPE == 65536, "register split");
+};
 constexpr int MAX_TILES = 1024;
 constexpr int BAR_TILES = 4;    // named barrier: the set-up warp -> the two producers
 constexpr int MAX_VIEWS = 64;
@@ -442,7 +445,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
   }
 
   if (warp >= 8 && warp < WARP_ROPE) {
-    tc::setmaxnreg_dec<REG_CTRL>();
+    tc::setmaxnreg_dec<RegSplit<FUSED>::CTRL>();
     if (warp == WARP_KTMA || warp == WARP_VTMA) {
       // -------------------------------------- producers of this CTA's halves
       const bool is_k = warp == WARP_KTMA;
@@ -601,7 +604,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
     }
   } else if (warp >= WARP_ROPE) {
     // ----------------------------------------------------------------- RoPE
-    tc::setmaxnreg_dec<REG_ROPE>();
+    tc::setmaxnreg_dec<RegSplit<FUSED>::ROPE>();
     const int rt = tid - WARP_ROPE * 32;   // 0..127
     constexpr int HALF = D / 2;
     // this CTA's 64 rows of every key tile, rotated in place once TMA has
@@ -680,7 +683,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
     }
   } else {
     // ------------------------------------------------- softmax + epilogue
-    tc::setmaxnreg_inc<REG_SOFTMAX>();
+    tc::setmaxnreg_inc<RegSplit<FUSED>::SOFTMAX>();
     const int i = warp >> 2;            // query tile
     const int lg = warp & 3;            // TMEM lane group of this warp
     const int row = lg * 32 + lane;
