@@ -264,3 +264,66 @@ def test_host_shape_limits_match_the_kernels():
     assert const("api.cu", "kMaxViews") == const("prefill_tc.cu", "MAX_VIEWS") == const("verify_tc.cu", "MAX_VIEWS")
     assert const("api.cu", "kPrefillMaxKeyTiles") == const("prefill_tc.cu", "MAX_TILES")
     assert const("api.cu", "kPrefillKeyTile") == const("prefill_tc.cu", "BN")
+
+
+def _sm_count():
+    """The SM count the library plans for: the device's, or 148 without one."""
+    try:
+        import torch
+        if torch.cuda.is_available():
+            return torch.cuda.get_device_properties(0).multi_processor_count
+    except Exception:
+        pass
+    return 148
+
+
+def _verify_plan(C, Hkv, G, blk, d, n_visual, tail_cap, n_sm):
+    """The verify partition, restated: the row form (64 or 128 block rows per
+    unit), the units' tiles of 64 keys spread over at most one wave (two CTAs
+    per SM for the 64-row form, one for the 128-row form), at least 4 tiles and
+    at most 14 whole units' worth per CTA, at most 64 pieces per unit.
+    Returns (tiles per unit, tiles per CTA, CTAs, pieces per unit at most,
+    units, rows per unit, workspace bytes)."""
+    R = blk * G
+    rows = 128 if R > 64 else 64
+    RH = -(-R // rows)
+    units = C * Hkv * RH
+    TM = -(-(n_visual + tail_cap) // 64)
+    total = units * TM
+    slots = (1 if rows == 128 else 2) * n_sm
+    if units <= slots < 2 * units:
+        W, n, P = TM, units, 1
+    else:
+        n = min(slots, -(-total // 4))
+        n = max(n, -(-units // 14))
+        n = min(n, total // max(1, (TM + 62) // 63))
+        n = max(n, 1)
+        W = -(-total // n)
+        n = -(-total // W)
+        P = -(-TM // W) + 1
+    RU = min(R, rows)
+    ws = 0 if W % TM == 0 else (units * 4 + 255) // 256 * 256 + units * P * RU * (d + 2) * 4
+    return TM, W, n, P, units, RU, ws
+
+
+@pytest.mark.parametrize("blk", [1, 9, 16, 17, 32, 33])
+@pytest.mark.parametrize("Hq", [8, 32, 64])
+def test_verify_plan_bounds_and_workspace(L, blk, Hq):
+    """Over batches, tail capacities and window sizes: every unit is cut into
+    at most 64 pieces and every CTA's share into at most 16 (the kernel's
+    tables), the one-wave rule holds, and the library's workspace size is the
+    plan's."""
+    Hkv, d, n_sm = 8, 128, _sm_count()
+    G = Hq // Hkv
+    for C in (1, 3, 8, 32, 64, 200, 1000):
+        for tail_cap, frames in ((64, (16, 1, 1, 32)), (128, (256, 4, 4, 180)), (1024, (512, 6, 8, 256))):
+            if blk > tail_cap:
+                continue
+            P, V, F, T = frames
+            TM, W, n, Pm, units, RU, ws = _verify_plan(C, Hkv, G, blk, d, P + V * F * T, tail_cap, n_sm)
+            assert Pm <= 64, (C, blk, Hq, tail_cap)
+            assert (W - 1) // TM + 2 <= 16 or Pm == 1, (C, blk, Hq, tail_cap)
+            assert n * W >= units * TM > (n - 1) * W
+            desc = _shape_desc(n_cache=C, n_view=V, n_frame=F, frame_len=T, prefix_len=P, tail_cap=tail_cap,
+                               n_kv_head=Hkv, head_dim=d)
+            assert L.skv_verify_workspace_bytes(ctypes.byref(desc), Hq, blk) == ws, (C, blk, Hq, tail_cap)
