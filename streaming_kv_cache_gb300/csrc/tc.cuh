@@ -97,6 +97,48 @@ __device__ __forceinline__ bool bounded_wait(Try try_fn, uint32_t bar, uint32_t 
   }
 }
 
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Barrier across every CTA of a cooperative launch (all of them are resident
+// at once, so a CTA that waits here never holds back one that has not
+// started).  count and gen are two words of global memory, count zero
+// between calls: each CTA's thread 0 arrives on count; the last to arrive
+// advances gen, which releases the others, and sets count back to zero
+// (before this kernel ends, so before any later call arrives).  The wait is
+// bounded by limit_ns of globaltimer; false when it ran out (some CTA did
+// not arrive).  Call from every thread of the CTA; flag is a shared-memory
+// word for the verdict.
+__device__ __forceinline__ bool grid_barrier(uint32_t* count, uint32_t* gen, uint32_t n_cta, uint64_t limit_ns,
+                                             volatile int* flag) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int ok = 1;
+    const uint32_t g0 = ld_acquire_gpu(gen);
+    __threadfence();
+    if (atomicAdd(count, 1u) == n_cta - 1) {
+      atomicAdd(gen, 1u);
+      atomicExch(count, 0u);
+    } else {
+      const uint64_t t0 = globaltimer();
+      while (ld_acquire_gpu(gen) == g0) {
+        if (globaltimer() - t0 > limit_ns) {
+          ok = 0;
+          break;
+        }
+        __nanosleep(64);
+      }
+    }
+    __threadfence();
+    *flag = ok;
+  }
+  __syncthreads();
+  return *flag != 0;
+}
+
 // Wait for the phase with the given parity to complete (bounded, see
 // bounded_wait).  A suspended try_wait may sleep up to the suspend hint, so a
 // limit far under the hint is not kept: kernels compiled with SW (chosen by

@@ -57,6 +57,12 @@ constexpr int MAX_VIEWS = 64;
 constexpr int MAX_PIECES = 16;   // pieces of one CTA's share
 constexpr int MAX_SPLITS = 64;   // pieces of one unit
 constexpr int MIN_SHARE = 4;     // key tiles per CTA at least
+// With this many pieces per unit at most or more, the units that pieces
+// share are merged by every CTA after a grid barrier (a cooperative launch);
+// with fewer, by each unit's last piece to arrive, which overlaps the merge
+// with the other CTAs' key loops (measured: the barrier costs more than it
+// saves at two pieces per unit, and saves a third of a batch-one call).
+constexpr int COOP_MIN_PIECES = 4;
 constexpr float RESCALE_THRESHOLD = 8.0f;
 constexpr uint64_t DRAIN_NS = 500000000ull;
 
@@ -156,6 +162,9 @@ struct VerifyParams {
   float* ws_o;                // [units * P_max][R][D]
   float* ws_ml;               // [units * P_max][R][2]
   int* ws_count;              // [units] arrival counters, zero between calls
+  int coop;                   // 1: cooperative launch, the merge runs after a grid barrier on every CTA
+  uint32_t* bar_count;        // grid barrier: arrivals (zero between calls) and generation
+  uint32_t* bar_gen;
   const float2* rope;
   const int32_t* head;
   int32_t* status;
@@ -262,6 +271,82 @@ __device__ __noinline__ void merge_pieces(const VerifyParams& p, int u, int n, i
   __syncthreads();
 }
 
+// The merge of every unit that more than one piece shares, spread over all
+// warps of a cooperative launch once every piece has left its partial: warp
+// gw of n_w takes (unit, row) pairs gw, gw + n_w, ...; lane k holds the (m, l)
+// of pieces k and k + 32, the row max and the weights go round by shuffles,
+// and lane i sums columns 4i .. 4i+3 over the pieces (eight loads in flight).
+// A row whose pieces all left l = 0 belongs to a skipped cache and is not
+// written.
+template <int D, bool WIDE>
+__device__ __noinline__ void merge_all(const VerifyParams& p, int gw, int n_w, int lane) {
+  constexpr int D4 = D / 4;
+  constexpr uint32_t FULL = 0xffffffffu;
+  static_assert(MAX_SPLITS <= 64, "two pieces per lane");
+  const float4* ws_o4 = reinterpret_cast<const float4*>(p.ws_o);
+  const float2* ws_ml2 = reinterpret_cast<const float2*>(p.ws_ml);
+  const long long pairs = (long long)p.units * p.RU;
+  for (long long e = gw; e < pairs; e += n_w) {
+    const int u = (int)(e / p.RU), row = (int)(e - (long long)u * p.RU);
+    const int plane = u / p.RH, row0 = (u % p.RH) * VCfg<WIDE>::ROWS;
+    if (row >= p.R - row0) continue;
+    const int f = first_cta(u, p.TM, p.W), n = last_cta(u, p.TM, p.W) - f + 1;
+    if (n <= 1) continue;                      // its one piece wrote the output
+    const size_t base = (size_t)u * p.P_max;
+    float mk[2], lk[2], M = -INFINITY;
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const int k = lane + 32 * q;
+      const float2 ml = k < n ? __ldcg(ws_ml2 + (base + k) * p.RU + row) : make_float2(-INFINITY, 0.f);
+      mk[q] = ml.x;
+      lk[q] = ml.y;
+      M = fmaxf(M, ml.x);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(FULL, M, o));
+    float wk[2], den = 0.f;
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      wk[q] = mk[q] == -INFINITY ? 0.f : exp2f(mk[q] - M);
+      den += wk[q] * lk[q];
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(FULL, den, o);
+    if (!(den > 0.f)) continue;
+    const float inv = 1.f / den;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int k0 = 0; k0 < n; k0 += 8) {
+      float w[8];
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        const int k = k0 + kk;
+        const float w0 = __shfl_sync(FULL, wk[0], k & 31), w1 = __shfl_sync(FULL, wk[1], k & 31);
+        w[kk] = k < n ? (k < 32 ? w0 : w1) * inv : 0.f;
+      }
+      float4 t[8];
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)
+        t[kk] = (lane < D4 && w[kk] != 0.f) ? __ldcg(ws_o4 + ((base + k0 + kk) * p.RU + row) * D4 + lane)
+                                            : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        acc.x += w[kk] * t[kk].x;
+        acc.y += w[kk] * t[kk].y;
+        acc.z += w[kk] * t[kk].z;
+        acc.w += w[kk] * t[kk].w;
+      }
+    }
+    if (lane < D4) {
+      const int c = plane / p.g.Hkv, h = plane % p.g.Hkv;
+      const int brow = row0 + row, jt = brow / p.G, gq = brow % p.G;
+      uint2 pk;
+      pk.x = pack_bf16x2(acc.x, acc.y);
+      pk.y = pack_bf16x2(acc.z, acc.w);
+      *reinterpret_cast<uint2*>(p.out + (((size_t)c * p.blk + jt) * p.Hq + h * p.G + gq) * D + lane * 4) = pk;
+    }
+  }
+}
+
 // SW: compiled for a wait limit under the suspend hint (see tc::bounded_wait)
 // TABLE: rope_mode 1 (a table row per key), see rotate_key_rows.
 template <int D, bool SW, bool WIDE, bool TABLE = false>
@@ -307,43 +392,49 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
       *s_abort = 0;
       s_info[1] = 0;
     }
-    // this CTA's share [g0, g1) of the units' tile sequence, cut at unit boundaries
+    // this CTA's share [g0, g1) of the units' tile sequence, cut at unit
+    // boundaries: piece l is unit u0 + l (its first tile ta, tiles before tb),
+    // one lane per piece, so that the pieces' checks load together
     const long long g0 = (long long)blockIdx.x * p.W;
     const long long g1 = min(g0 + p.W, (long long)p.units * p.TM);
-    int n = 0, gsum = 0;
-    for (long long gg = g0; gg < g1 && n < MAX_PIECES;) {
-      const int u = (int)(gg / p.TM);
-      const int ta = (int)(gg - (long long)u * p.TM);
+    const int u0 = (int)(g0 / p.TM);
+    const int n = g1 > g0 ? min(MAX_PIECES, (int)((g1 - 1) / p.TM) - u0 + 1) : 0;
+    int nt = 0;
+    if (lane < n) {
+      const int u = u0 + lane;
+      const int ta = lane == 0 ? (int)(g0 - (long long)u0 * p.TM) : 0;
       const int tb = (int)min((long long)p.TM, g1 - (long long)u * p.TM);
       const int c = u / p.RH / g.Hkv;
-      // unit checks, one lane per view: ring heads in range, tail within its capacity
+      // unit checks: ring heads in range, tail within its capacity
       const int tl = p.tail_len[c];
       bool head_ok = true;
-      for (int v = lane; v < g.V; v += 32) {
+#pragma unroll 4
+      for (int v = 0; v < g.V; ++v) {
         const int hv = p.head[(size_t)c * g.V + v];
         head_ok = head_ok && hv >= 0 && hv < g.F;
       }
-      head_ok = __all_sync(0xffffffffu, head_ok);
       const bool ok = head_ok && tl >= 0 && tl + p.blk <= g.tail_cap;
       const int nt_unit = (g.n_visual() + tl + p.blk + BN - 1) / BN;
-      const int nt = ok ? max(0, min(tb, nt_unit) - ta) : 0;
-      if (lane == 0) {
-        int* pc = s_piece + n * 8;
-        pc[PC_U] = u;
-        pc[PC_TA] = ta;
-        pc[PC_NT] = nt;
-        pc[PC_TL] = ok ? tl : 0;
-        pc[PC_K] = (int)blockIdx.x - first_cta(u, p.TM, p.W);
-        pc[PC_N] = last_cta(u, p.TM, p.W) - first_cta(u, p.TM, p.W) + 1;
-        pc[PC_OK] = ok;
-        pc[PC_G0] = gsum;
-        // the tail's own checks are reported by the tail write
-        if (!head_ok && ta == 0) set_status(p.status, SKV_DEV_BAD_HEAD);
-      }
-      gsum += nt;
-      ++n;
-      gg = (long long)u * p.TM + tb;
+      nt = ok ? max(0, min(tb, nt_unit) - ta) : 0;
+      int* pc = s_piece + lane * 8;
+      pc[PC_U] = u;
+      pc[PC_TA] = ta;
+      pc[PC_NT] = nt;
+      pc[PC_TL] = ok ? tl : 0;
+      pc[PC_K] = (int)blockIdx.x - first_cta(u, p.TM, p.W);
+      pc[PC_N] = last_cta(u, p.TM, p.W) - first_cta(u, p.TM, p.W) + 1;
+      pc[PC_OK] = ok;
+      // the tail's own checks are reported by the tail write
+      if (!head_ok && ta == 0) set_status(p.status, SKV_DEV_BAD_HEAD);
     }
+    // tiles of the pieces before each (exclusive prefix sum over the lanes)
+    int incl = nt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += t;
+    }
+    if (lane < n) s_piece[lane * 8 + PC_G0] = incl - nt;
     if (lane == 0) {
       s_info[0] = n;
       tc::fence_barrier_init();
@@ -603,7 +694,16 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
     int gt = 0, a = 0;
     bool alive = true;
     for (int pi = 0; alive && pi < n_pieces; ++pi) {
-      if (!P(pi, PC_OK)) continue;      // a skipped cache: no piece of its units arrives
+      if (!P(pi, PC_OK)) {
+        // a skipped cache: without a grid barrier no piece of its units
+        // arrives; with one, the merge finds l = 0 in every piece and skips it
+        if (p.coop && P(pi, PC_N) > 1 && (P(pi, PC_U) % p.RH) * C::ROWS + row < p.R) {
+          const size_t sl = (size_t)P(pi, PC_U) * p.P_max + P(pi, PC_K);
+          p.ws_ml[(sl * p.RU + row) * 2] = -INFINITY;
+          p.ws_ml[(sl * p.RU + row) * 2 + 1] = 0.f;
+        }
+        continue;
+      }
       const int nt = P(pi, PC_NT), u = P(pi, PC_U), n_unit = P(pi, PC_N);
       const int plane = u / p.RH, c = plane / g.Hkv, h = plane % g.Hkv;
       const int brow = (u % p.RH) * C::ROWS + row;   // block row of this lane
@@ -643,7 +743,8 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
           m4[(k >> 1) & 3] = fmax3(m4[(k >> 1) & 3], __uint_as_float(v[k]), __uint_as_float(v[k + 1]));
         float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
         mx *= sl;
-        const bool grow = j > 0 && mx > m_used + RESCALE_THRESHOLD;
+        // (rows past the block hold no query: they never ask for a rescale)
+        const bool grow = valid && j > 0 && mx > m_used + RESCALE_THRESHOLD;
         if (j == 0) {
           m_used = (mx == -INFINITY) ? 0.f : mx;
         } else if (__any_sync(0xffffffffu, grow)) {
@@ -757,7 +858,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
           p.ws_ml[(slot * p.RU + row) * 2 + 1] = nt > 0 ? l : 0.f;
         }
         asm volatile("bar.sync 1, %0;" ::"r"(SOFTMAX_THREADS) : "memory");
-        if (tid == 0) {
+        if (tid == 0 && !p.coop) {
           __threadfence();
           const int prev = atomicAdd(&p.ws_count[u], 1);
           if (prev == n_unit - 1) {
@@ -780,6 +881,15 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
   if (warp == WARP_KTMA) {
     tc::tc_fence_after();
     tc::tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+  if (p.coop) {
+    // every CTA's partials are in the workspace once all have arrived here;
+    // then all warps of the grid merge the units that pieces share
+    if (tc::grid_barrier(p.bar_count, p.bar_gen, gridDim.x, wait_ns, s_info + 12))
+      merge_all<D, WIDE>(p, (int)blockIdx.x * (C::NT / 32) + warp, (int)gridDim.x * (C::NT / 32), lane);
+    else if (tid == 0)
+      set_status(p.status, SKV_DEV_TIMEOUT);
+    return;
   }
   // units whose last piece this CTA held: the K/V stages are idle now and hold
   // the merge weights
@@ -808,17 +918,24 @@ int num_sms() {
   return n;
 }
 
-// Raise the kernel's dynamic shared-memory limit once per device.
+// Raise the kernel's dynamic shared-memory limit once per device and return
+// how many of its CTAs one SM holds (asked once per device as well).
 template <typename K>
-cudaError_t set_smem_once(K kernel, int bytes, int variant) {
-  static std::atomic<int> done[64][10];
+cudaError_t set_smem_once(K kernel, int bytes, int threads, int variant, int* per_sm) {
+  static std::atomic<int> occ[64][10];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev >= 0 && dev < 64 && done[dev][variant].load(std::memory_order_relaxed)) return cudaSuccess;
+  if (dev >= 0 && dev < 64 && (*per_sm = occ[dev][variant].load(std::memory_order_relaxed)) > 0)
+    return cudaSuccess;
   e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-  if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev][variant].store(1, std::memory_order_relaxed);
-  return e;
+  if (e != cudaSuccess) return e;
+  int n = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, bytes);
+  if (e != cudaSuccess) return e;
+  *per_sm = n;
+  if (dev >= 0 && dev < 64 && n > 0) occ[dev][variant].store(n, std::memory_order_relaxed);
+  return cudaSuccess;
 }
 
 struct VerifyPlan {
@@ -875,9 +992,12 @@ int row_halves(int Hq, int Hkv, int blk) {
   return (blk * (Hq / Hkv) + rows - 1) / rows;
 }
 
-// Workspace: [units] int32 counters (256-byte aligned block), then the fp32
-// partial O rows and the (m, l) pairs of units x P_max piece slots, each slot
-// holding a unit's (at most ROWS of the form) rows.
+// Workspace: [units] int32 arrival counters and the grid barrier's two words
+// (a 256-byte aligned block), then the fp32 partial O rows and the (m, l)
+// pairs of units x P_max piece slots, each slot holding a unit's (at most
+// ROWS of the form) rows.
+size_t ws_header_bytes(size_t units) { return ((units + 2) * 4 + 255) / 256 * 256; }
+
 size_t verify_ws_bytes(const Geom& g, int Hq, int blk) {
   const bool wide = verify_wide(Hq, g.Hkv, blk);
   const int RH = row_halves(Hq, g.Hkv, blk);
@@ -885,7 +1005,7 @@ size_t verify_ws_bytes(const Geom& g, int Hq, int blk) {
   const size_t units = (size_t)g.C * g.Hkv * RH;
   if (units == 0 || all_single(pl, (long long)units)) return 0;
   const size_t rows = units * pl.P_max * min(blk * (Hq / g.Hkv), wide ? VCfg<true>::ROWS : VCfg<false>::ROWS);
-  return (units * 4 + 255) / 256 * 256 + rows * (g.d + 2) * sizeof(float);
+  return ws_header_bytes(units) + rows * (g.d + 2) * sizeof(float);
 }
 
 cudaError_t make_kv_tmaps(const Geom& g, const void* k, const void* vt, int k_box_rows, int v_box_rows,
@@ -942,29 +1062,43 @@ cudaError_t launch_verify_tc(const Geom& g, int Hq, int blk, const int32_t* tail
   if (ws_bytes < need || (need && !ws)) return cudaErrorInvalidValue;
   const size_t n_rows = units * p.P_max * p.RU;
   p.ws_count = static_cast<int*>(ws);
-  p.ws_o = need ? reinterpret_cast<float*>(static_cast<char*>(ws) + (units * 4 + 255) / 256 * 256) : nullptr;
+  p.ws_o = need ? reinterpret_cast<float*>(static_cast<char*>(ws) + ws_header_bytes(units)) : nullptr;
   p.ws_ml = need ? p.ws_o + n_rows * g.d : nullptr;
+  p.bar_count = need ? reinterpret_cast<uint32_t*>(ws) + units : nullptr;
+  p.bar_gen = need ? p.bar_count + 1 : nullptr;
   p.rope = reinterpret_cast<const float2*>(rope);
   p.head = head;
   p.status = status;
   p.scale_log2 = sm_scale * 1.4426950408889634f;
   p.wait_ns = wait_ns ? wait_ns : 2000000000ull;
-  // launched as a programmatic dependent of the tail write before it: set-up,
-  // query blocks and visual key tiles overlap that kernel, whose writes the
-  // producers wait for before they load a tile that reaches the tail
+  // When pieces share units and the grid fits on the GPU at once, the launch
+  // is cooperative: every CTA waits at a grid barrier for all partials, then
+  // all of them merge.  Otherwise the last piece of a unit to arrive merges
+  // it, and the launch is a programmatic dependent of the tail write before
+  // it (set-up, query blocks and visual key tiles overlap that kernel, whose
+  // writes the producers wait for before they load a tile that reaches the
+  // tail).
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.gridDim = dim3((unsigned)pl.n_cta);
-  cfg.blockDim = dim3(wide ? VCfg<true>::NT : VCfg<false>::NT);
+  const int n_threads = wide ? VCfg<true>::NT : VCfg<false>::NT;
+  cfg.blockDim = dim3(n_threads);
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   const bool sw = p.wait_ns < tc::kSuspendHintNs;
   auto launch = [&](auto kernel, int smem, int variant) -> cudaError_t {
-    cudaError_t err = set_smem_once(kernel, smem, variant);
+    int per_sm = 0;
+    cudaError_t err = set_smem_once(kernel, smem, n_threads, variant, &per_sm);
     if (err != cudaSuccess) return err;
+    p.coop = need > 0 && pl.P_max >= COOP_MIN_PIECES && (long long)pl.n_cta <= (long long)per_sm * num_sms();
+    if (p.coop) {
+      attr[0].id = cudaLaunchAttributeCooperative;
+      attr[0].val.cooperative = 1;
+    } else {
+      attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      attr[0].val.programmaticStreamSerializationAllowed = 1;
+    }
     cfg.dynamicSmemBytes = smem;
     return cudaLaunchKernelEx(&cfg, kernel, tk, tv, tq, p);
   };

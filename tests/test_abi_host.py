@@ -302,7 +302,7 @@ def _verify_plan(C, Hkv, G, blk, d, n_visual, tail_cap, n_sm):
         n = -(-total // W)
         P = -(-TM // W) + 1
     RU = min(R, rows)
-    ws = 0 if W % TM == 0 else (units * 4 + 255) // 256 * 256 + units * P * RU * (d + 2) * 4
+    ws = 0 if W % TM == 0 else ((units + 2) * 4 + 255) // 256 * 256 + units * P * RU * (d + 2) * 4
     return TM, W, n, P, units, RU, ws
 
 

@@ -174,6 +174,51 @@ def test_verify_alpamayo_batches(B):
     assert pair.cache.device_status() == 0
 
 
+@pytest.mark.parametrize("B,blk", [(1, 9), (8, 9), (1, 17)])
+def test_verify_merge_after_grid_barrier_repeats_and_captures(B, blk):
+    """Small batches spread each unit over many pieces, and the partials are
+    merged by every CTA after a grid barrier (a cooperative launch).  Three
+    calls on one workspace (the barrier's words go back to their start state
+    after each) and a CUDA-graph replay of the same call give bit-identical
+    outputs, within the tolerance of the oracle."""
+    w = W["alpamayo_verify"].with_(C=B, blk=blk)
+    watch = list(range(B)) if B <= 2 else [0, 3, 7]
+    pair = Pair(w, "vg%d_%d" % (B, blk), watch=watch)
+    pair.fill()
+    pair.insert()
+    pair.set_tail(w.tail_len)
+    q, k, v = synth.verify_block(w, pair.tag)
+    tail = torch.full((B,), w.tail_len, dtype=torch.int32, device="cuda")
+    dq, dk, dv = to_dev(q), to_dev(k), to_dev(v)
+    ws = skv.verify_workspace(pair.cache, w.Hq, w.blk)
+    assert ws.numel() > 0                       # pieces share units
+    outs = []
+    for _ in range(3):
+        out, _, _ = skv.stream_attn_verify(pair.cache, tail, dq, dk, dv, w.sm_scale, ws=ws)
+        outs.append(out.clone())
+    for o in outs[1:]:
+        assert torch.equal(o, outs[0])
+    got = bf16_dev_to_f64(outs[0])
+    for c in watch:
+        want, _ = O.stream_verify(pair.win[c], q[c], k[c], v[c], w.theta, w.sm_scale)
+        assert_close(got[c], want, "verify B=%d blk %d cache %d" % (B, blk, c))
+    # captured into a graph and replayed twice
+    gout = torch.empty_like(outs[0])
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g):
+            skv.stream_attn_verify(pair.cache, tail, dq, dk, dv, w.sm_scale, ws=ws, out=gout)
+    torch.cuda.current_stream().wait_stream(side)
+    for _ in range(2):
+        gout.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(gout, outs[0])
+    assert pair.cache.device_status() == 0
+
+
 def test_verify_full_block_rows_uneven_tails():
     """64 block rows per kv head (blk 16, 4 query heads per kv head) and a
     different tail length per cache: units end at different key tiles, so
