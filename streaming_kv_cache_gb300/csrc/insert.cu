@@ -16,6 +16,8 @@
 // The verify block's tail write also computes the greedy accept length (it
 // needs only the token ids) and lets the attention kernel that follows launch
 // early: that kernel waits for this one's writes only before it reads tail rows.
+#include <atomic>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -168,6 +170,18 @@ cudaError_t launch_write_rows(const Geom& g, void* k, void* vt, const void* k_sr
   auto* vv = static_cast<uint16_t*>(vt);
   auto* ks = static_cast<const uint16_t*>(k_src);
   auto* vs = static_cast<const uint16_t*>(v_src);
+  {
+    // the same shared-memory carve-out as the attention kernel that may
+    // follow as a programmatic dependent, so that its CTAs can land on SMs
+    // that still run this kernel's
+    static std::atomic<int> done[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < 64 && !done[dev].load(std::memory_order_relaxed)) {
+      cudaFuncSetAttribute(write_rows_kernel<128>, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+      cudaFuncSetAttribute(write_rows_kernel<64>, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+      done[dev].store(1, std::memory_order_relaxed);
+    }
+  }
   if (g.d == 128)
     write_rows_kernel<128><<<(unsigned)blocks, THREADS, 0, st>>>(g, kk, vv, ks, vs, n_group, n_tok, mode,
                                                              row0, head, sync, tail_len, status, acc);

@@ -1079,7 +1079,7 @@ cudaError_t launch_verify_tc(const Geom& g, int Hq, int blk, const int32_t* tail
   // writes the producers wait for before they load a tile that reaches the
   // tail).
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   cfg.gridDim = dim3((unsigned)pl.n_cta);
   const int n_threads = wide ? VCfg<true>::NT : VCfg<false>::NT;
   cfg.blockDim = dim3(n_threads);
@@ -1092,15 +1092,20 @@ cudaError_t launch_verify_tc(const Geom& g, int Hq, int blk, const int32_t* tail
     cudaError_t err = set_smem_once(kernel, smem, n_threads, variant, &per_sm);
     if (err != cudaSuccess) return err;
     p.coop = need > 0 && pl.P_max >= COOP_MIN_PIECES && (long long)pl.n_cta <= (long long)per_sm * num_sms();
-    if (p.coop) {
-      attr[0].id = cudaLaunchAttributeCooperative;
-      attr[0].val.cooperative = 1;
-    } else {
-      attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-      attr[0].val.programmaticStreamSerializationAllowed = 1;
-    }
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeCooperative;
+    attr[1].val.cooperative = 1;
+    cfg.numAttrs = p.coop ? 2 : 1;
     cfg.dynamicSmemBytes = smem;
-    return cudaLaunchKernelEx(&cfg, kernel, tk, tv, tq, p);
+    cudaError_t le = cudaLaunchKernelEx(&cfg, kernel, tk, tv, tq, p);
+    if (le != cudaSuccess && p.coop) {
+      cudaGetLastError();
+      attr[0] = attr[1];
+      cfg.numAttrs = 1;
+      le = cudaLaunchKernelEx(&cfg, kernel, tk, tv, tq, p);
+    }
+    return le;
   };
   const bool table = g.d == 128 && !sw && !g.rope_steps;
   if (table) {
