@@ -353,6 +353,11 @@ size_t skv_verify_workspace_bytes(const skv_cache* cache, int32_t n_q_head, int3
  *     next one (re-zero it after a call that set a device status bit).
  *     Calls that may run at the same time (other streams) need workspaces
  *     of their own: the arrival counters in it are per call.
+ * Small batches spread each (cache, kv head)'s keys over many CTAs; when
+ * four or more share one and the grid fits on the GPU at once, the call is
+ * a cooperative launch whose CTAs meet once at a grid barrier (its wait is
+ * bounded by cache->wait_ns and ends in SKV_DEV_TIMEOUT); such a launch
+ * starts only when the whole grid can be resident.
  * Needs 1 <= blk <= tail_cap, V <= 64 and Hq/Hkv <= 64 (else
  * SKV_ERR_UNSUPPORTED).  A block of up to 128 rows per kv head
  * (blk * Hq/Hkv) streams the keys once; a larger one is taken 128 rows at a
