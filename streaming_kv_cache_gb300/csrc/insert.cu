@@ -38,7 +38,9 @@ struct AcceptArgs {
   int32_t* next_token;
 };
 
-template <int D>
+// TAIL: the instance that serves the verify block's tail writes, which asks
+// for its own shared-memory carve-out (below); the code is the same.
+template <int D, bool TAIL>
 __global__ void __launch_bounds__(THREADS) write_rows_kernel(
     Geom g, uint16_t* __restrict__ k, uint16_t* __restrict__ vt,
     const uint16_t* __restrict__ k_src, const uint16_t* __restrict__ v_src, int n_group,
@@ -170,24 +172,29 @@ cudaError_t launch_write_rows(const Geom& g, void* k, void* vt, const void* k_sr
   auto* vv = static_cast<uint16_t*>(vt);
   auto* ks = static_cast<const uint16_t*>(k_src);
   auto* vs = static_cast<const uint16_t*>(v_src);
-  {
+  if (mode == MODE_TAIL) {
     // the same shared-memory carve-out as the attention kernel that may
     // follow as a programmatic dependent, so that its CTAs can land on SMs
-    // that still run this kernel's
+    // that still run this kernel's (the other writes keep the default: the
+    // frame insert ran 14% slower with it)
     static std::atomic<int> done[64];
     int dev = 0;
     if (cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < 64 && !done[dev].load(std::memory_order_relaxed)) {
-      cudaFuncSetAttribute(write_rows_kernel<128>, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
-      cudaFuncSetAttribute(write_rows_kernel<64>, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+      cudaFuncSetAttribute(write_rows_kernel<128, true>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           cudaSharedmemCarveoutMaxShared);
+      cudaFuncSetAttribute(write_rows_kernel<64, true>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           cudaSharedmemCarveoutMaxShared);
       done[dev].store(1, std::memory_order_relaxed);
     }
   }
+  auto launch = [&](auto kernel) {
+    kernel<<<(unsigned)blocks, THREADS, 0, st>>>(g, kk, vv, ks, vs, n_group, n_tok, mode, row0, head, sync, tail_len,
+                                                 status, acc);
+  };
   if (g.d == 128)
-    write_rows_kernel<128><<<(unsigned)blocks, THREADS, 0, st>>>(g, kk, vv, ks, vs, n_group, n_tok, mode,
-                                                             row0, head, sync, tail_len, status, acc);
+    mode == MODE_TAIL ? launch(write_rows_kernel<128, true>) : launch(write_rows_kernel<128, false>);
   else
-    write_rows_kernel<64><<<(unsigned)blocks, THREADS, 0, st>>>(g, kk, vv, ks, vs, n_group, n_tok, mode,
-                                                            row0, head, sync, tail_len, status, acc);
+    mode == MODE_TAIL ? launch(write_rows_kernel<64, true>) : launch(write_rows_kernel<64, false>);
   return cudaGetLastError();
 }
 
