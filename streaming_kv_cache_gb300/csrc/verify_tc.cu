@@ -14,8 +14,10 @@
 // (a split in the manner of stream-K).  A CTA's share falls into pieces at
 // unit boundaries; a unit that one piece covers is written straight to the
 // output, otherwise every piece leaves an unnormalised fp32 partial (O,
-// running max m, sum l) in the workspace and the piece that arrives last
-// merges them after its CTA's key loop.
+// running max m, sum l) in the workspace.  With few pieces per unit the
+// piece that arrives last merges them after its CTA's key loop; with many
+// (small batches) the launch is cooperative, every CTA meets at a grid
+// barrier once its partials are out, and all warps of the grid merge.
 //
 // Per piece the query buffer holds the unit's blk x G block rows in its 64
 // rows (the WIDE form below: 128); the M=128 MMA reads rows past them from
