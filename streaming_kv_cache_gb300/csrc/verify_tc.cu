@@ -59,11 +59,12 @@ constexpr int MAX_VIEWS = 64;
 constexpr int MAX_PIECES = 16;   // pieces of one CTA's share
 constexpr int MAX_SPLITS = 64;   // pieces of one unit
 constexpr int MIN_SHARE = 4;     // key tiles per CTA at least
-// With this many pieces per unit at most or more, the units that pieces
-// share are merged by every CTA after a grid barrier (a cooperative launch);
-// with fewer, by each unit's last piece to arrive, which overlaps the merge
-// with the other CTAs' key loops (measured: the barrier costs more than it
-// saves at two pieces per unit, and saves a third of a batch-one call).
+// When a unit may be cut into this many pieces or more (P_max), the units
+// that pieces share are merged by every CTA after a grid barrier (a
+// cooperative launch); with fewer, by each unit's last piece to arrive,
+// which overlaps the merge with the other CTAs' key loops (measured: the
+// barrier costs more than it saves at two pieces per unit, and saves a third
+// of a batch-one call).
 constexpr int COOP_MIN_PIECES = 4;
 constexpr float RESCALE_THRESHOLD = 8.0f;
 constexpr uint64_t DRAIN_NS = 500000000ull;
