@@ -345,6 +345,56 @@ def run_reference(args, rank, world):
                   "d2h_bytes_per_step": 0}})
 
 
+def small_batch_verify(skv, torch, dev, randn, reps: int = 3, calls: int = 20) -> dict:
+    """The verify call alone at batch 1 and 8 (the pages' deployment is batch
+    one): a cache per batch set up as the bench's, each call captured 20 times
+    into a CUDA graph and replayed; the median device time per call and the
+    algorithmic bytes per second.  The 13 MB of a batch-one cache stay in L2
+    between the replayed calls, so these are latency figures."""
+    res = {}
+    for B in (1, 8):
+        w = VERIFY_W.with_(C=B)
+        cache = skv.StreamCache(w.C, w.P, w.V, w.F, w.T, w.Hkv, w.d, w.theta, tail_cap=w.tail_cap)
+        skv.kv_write_rows(cache, 0, randn((w.C, w.P, w.Hkv, w.d)), randn((w.C, w.P, w.Hkv, w.d)))
+        for _ in range(w.F):
+            skv.kv_stream_insert(cache, randn((w.C, w.V, w.T, w.Hkv, w.d)), randn((w.C, w.V, w.T, w.Hkv, w.d)))
+        skv.kv_write_rows(cache, cache.n_visual, randn((w.C, w.tail_len, w.Hkv, w.d)),
+                          randn((w.C, w.tail_len, w.Hkv, w.d)))
+        qb = randn((w.C, w.blk, w.Hq, w.d), w.q_scale)
+        kb = randn((w.C, w.blk, w.Hkv, w.d))
+        vb = randn((w.C, w.blk, w.Hkv, w.d))
+        tail = torch.full((w.C,), w.tail_len, dtype=torch.int32, device=dev)
+        ws = skv.verify_workspace(cache, w.Hq, w.blk)
+        out = torch.empty_like(qb)
+        for _ in range(3):
+            skv.stream_attn_verify(cache, tail, qb, kb, vb, w.sm_scale, ws=ws, out=out)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(graph):
+                for _ in range(calls):
+                    skv.stream_attn_verify(cache, tail, qb, kb, vb, w.sm_scale, ws=ws, out=out)
+        torch.cuda.current_stream().wait_stream(side)
+        graph.replay()
+        torch.cuda.synchronize()
+        ms = []
+        for _ in range(reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            graph.replay()
+            b.record()
+            torch.cuda.synchronize()
+            ms.append(a.elapsed_time(b) / calls)
+        if cache.device_status():
+            raise RuntimeError("device status %d" % cache.device_status())
+        med = statistics.median(ms)
+        res["B%d" % B] = {"us": med * 1e3, "gbs": verify_bytes(w) / (med * 1e-3) / 1e9}
+        del cache, graph
+    return res
+
+
 def run_only(args):
     """One kernel alone on a reduced case (for ncu captures): scale-up
     geometry with --layers caches for prefill/insert/window/tail, the verify
@@ -723,6 +773,12 @@ def main():
         raise RuntimeError("device status %d in the end-to-end loops: %s" % (status, skv.status_string(status)))
     e2e_check = check_pipelined(torch, e2e_pipelined, step, dev_in, dev_out, ins, outs, [pc.head, vc.head])
 
+    # the verify call alone at batch 1 and 8 (reported beside the step, untimed by it)
+    try:
+        small = small_batch_verify(skv, torch, dev, randn)
+    except Exception as exc:  # a failure here must not cost the step's line
+        small = {"error": str(exc)[:200]}
+
     t_ms, e2e_ms, serial_ms = max_over_ranks(dist, [t_ms, e2e_ms, serial_ms], dev)
 
     flop = prefill_flop(pw)
@@ -762,6 +818,11 @@ def main():
                                 "frac": ins_gbs / pk["hbm_gbs"], "peak_source": tag,
                                 "ms": ins_ms, "inputs": "3 rotating input sets of 453 MB each, "
                                                         "larger than L2"},
+            "verify_small_batch": dict(small, note="one verify call (tail write + attention) at batch 1 "
+                                                   "and 8, 9-token block, graph replay of 20 calls, median "
+                                                   "of 3; the cache stays in L2 between calls",
+                                       hbm_frac={k: v["gbs"] / pk["hbm_gbs"] for k, v in small.items()
+                                                 if isinstance(v, dict)}),
             "fused_prefill_insert": {"ms": fz_ms, "tflops": flop / (fz_ms * 1e-3) / 1e12,
                                      "vs_insert_plus_prefill_ms": k_ms["insert"] + k_ms["prefill"],
                                      "note": "insert and prefill as one kernel, same results bit for bit; "
