@@ -312,7 +312,9 @@ def test_verify_plan_bounds_and_workspace(L, blk, Hq):
     """Over batches, tail capacities and window sizes: every unit is cut into
     at most 64 pieces and every CTA's share into at most 16 (the kernel's
     tables), the one-wave rule holds, and the library's workspace size is the
-    plan's."""
+    plan's.  Whenever a unit may be cut into four pieces or more (the plans
+    that ask for the merge after a grid barrier, a cooperative launch), the
+    grid fits one wave of the form's CTAs per SM."""
     Hkv, d, n_sm = 8, 128, _sm_count()
     G = Hq // Hkv
     for C in (1, 3, 8, 32, 64, 200, 1000):
@@ -324,6 +326,8 @@ def test_verify_plan_bounds_and_workspace(L, blk, Hq):
             assert Pm <= 64, (C, blk, Hq, tail_cap)
             assert (W - 1) // TM + 2 <= 16 or Pm == 1, (C, blk, Hq, tail_cap)
             assert n * W >= units * TM > (n - 1) * W
+            if Pm >= 4:
+                assert n <= (1 if blk * G > 64 else 2) * n_sm, (C, blk, Hq, tail_cap)
             desc = _shape_desc(n_cache=C, n_view=V, n_frame=F, frame_len=T, prefix_len=P, tail_cap=tail_cap,
                                n_kv_head=Hkv, head_dim=d)
             assert L.skv_verify_workspace_bytes(ctypes.byref(desc), Hq, blk) == ws, (C, blk, Hq, tail_cap)
