@@ -1103,6 +1103,8 @@ cudaError_t launch_verify_tc(const Geom& g, int Hq, int blk, const int32_t* tail
     cfg.dynamicSmemBytes = smem;
     cudaError_t le = cudaLaunchKernelEx(&cfg, kernel, tk, tv, tq, p);
     if (le != cudaSuccess && p.coop) {
+      // a driver that refuses the pair of attributes: a cooperative launch
+      // alone (the refusal is a launch-argument error, cleared here)
       cudaGetLastError();
       attr[0] = attr[1];
       cfg.numAttrs = 1;
